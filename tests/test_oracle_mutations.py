@@ -1,0 +1,81 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that
+the pins catch every one.  Each mutant is compiled on the CPU into a temporary
+directory; the real oracle is untouched."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.c")
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("causal mask includes no diagonal", "if (causal && j > i)", "if (causal && j >= i)"),
+    ("causal mask off", "if (causal && j > i)", "if (causal && j > i + N)"),
+    ("scale dropped from scores", "s_row[j] = scale * acc;", "s_row[j] = acc;"),
+    ("no max shift", "if (s_row[j] > m) m = s_row[j];", "if (s_row[j] > m) m = 0.0;"),
+    ("softmax not normalised", "for (long j = 0; j < N; ++j) p_row[j] /= denom;", ";"),
+    ("lse misses the max", "*lse_i = m + log(denom);", "*lse_i = log(denom);"),
+    ("output uses keys instead of values", "const double* vj = v + j * D;\n        for (long d = 0; d < D; ++d) o_i[d]",
+     "const double* vj = k + j * D;\n        for (long d = 0; d < D; ++d) o_i[d]"),
+    ("dP uses keys", "for (long d = 0; d < D; ++d) acc += doi[d] * vj[d];",
+     "for (long d = 0; d < D; ++d) acc += doi[d] * (k + j * D)[d];"),
+    ("dS drops Di", "ds_row[j] = p_row[j] * (ds_row[j] - di);", "ds_row[j] = p_row[j] * ds_row[j];"),
+    ("dS wrong sign", "ds_row[j] = p_row[j] * (ds_row[j] - di);", "ds_row[j] = p_row[j] * (di - ds_row[j]);"),
+    ("Di block-local partial sum", "for (long j = 0; j < N; ++j) di += p_row[j] * ds_row[j];",
+     "for (long j = 0; j < (N + 1) / 2; ++j) di += p_row[j] * ds_row[j];"),
+    ("dQ uses values", "const double* kj = k + j * D;\n            for (long d = 0; d < D; ++d) dq_i[d]",
+     "const double* kj = v + j * D;\n            for (long d = 0; d < D; ++d) dq_i[d]"),
+    ("dQ misses scale", "for (long d = 0; d < D; ++d) dq_i[d] *= scale;", ";"),
+    ("dK misses scale", "for (long d = 0; d < D; ++d) dkj[d] *= scale;", ";"),
+    ("dV uses dS", "double p = p_all[(size_t)r * N + j];", "double p = ds_all[(size_t)r * N + j];"),
+    ("dK uses dO", "const double* qi = q + i * D;\n                    for", "const double* qi = dout + i * D;\n                    for"),
+]
+
+
+def run_pins():
+    """A battery of pins; returns the names of the ones that fail."""
+    failed = []
+    checks = [
+        ("brute_force", lambda: pins.test_brute_force_tiny(5, 2, True)),
+        ("brute_force_nc", lambda: pins.test_brute_force_tiny(7, 4, False)),
+        ("row_sums", lambda: pins.test_probability_rows_sum_to_one_and_respect_mask(True)),
+        ("zero_scale", lambda: pins.test_zero_scale_is_mean_of_visible_values(True)),
+        ("large_scores", pins.test_large_scores_concentrate_on_the_argmax_without_overflow),
+        ("sdpa_c", lambda: pins.test_matches_torch_sdpa_float64_forward_and_gradients(19, 8, True)),
+        ("sdpa_nc", lambda: pins.test_matches_torch_sdpa_float64_forward_and_gradients(19, 8, False)),
+        ("finite_diff", lambda: pins.test_gradients_by_central_differences(4, 3, True)),
+        ("invariants", lambda: pins.test_gradient_invariants_and_di_identity(True)),
+    ]
+    for name, fn in checks:
+        try:
+            with np.errstate(all="ignore"):
+                fn()
+        except Exception:  # an assertion, or NaNs tripping one
+            failed.append(name)
+    return failed
+
+
+def test_unmutated_oracle_passes_the_battery():
+    assert run_pins() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, old, new, tmp_path, monkeypatch):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    mutated = src.replace(old, new, 1)
+    assert mutated != src
+    shutil.copy(os.path.join(os.path.dirname(SRC), "fa_oracle.h"), tmp_path / "fa_oracle.h")
+    (tmp_path / "fa_oracle.c").write_text(mutated)
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-o", str(so),
+                    str(tmp_path / "fa_oracle.c"), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle._bind(str(so)))
+    failed = run_pins()
+    assert failed, f"no pin caught the planted mistake: {name}"
