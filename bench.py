@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward + backward through libfattn on GB300.
+
+One step is the whole path on one batch of seeded synthetic input already in
+HBM: fa_fwd, then the backward stages (Di preprocess, dK/dV with atomic dQ,
+dQ convert), exactly what fa_bwd enqueues.  The default workload is the
+long-sequence causal case B1 H8 N65536 D128 bf16; every input tensor
+(134 MB) is larger than the 129 MB L2, so no flush is needed between steps.
+
+Throughput is FLOP/s with the method's own count: 4*B*H*N^2*D for the
+forward, 2.5x that for the backward, halved under the causal mask.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed alone
+
+Several GPUs (torchrun, one rank per GPU): every rank runs its own replica
+of the workload (independent problems, no data exchange); the value is all
+ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd on 1×GB300; % of dense BF16 tensor peak"
+DOMINANT = "bwd_dkdv"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long64k_causal")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the two-pass deterministic backward instead of atomic dQ")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the forward-only long-context measurement")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# environment helpers
+# --------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    """Measured dense bf16 peaks (TFLOP/s) and HBM GB/s, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"burst": float(d["bf16_tflops"]), "sustained": float(d["bf16_tflops_sustained"]),
+                "hbm": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"burst": 1900.0, "sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "exact_attention_93_gb300", "csrc"))):
+        h.update(open(os.path.join(ROOT, "exact_attention_93_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    for line in open(p):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+            try:
+                return float(cells[2]) if cells[3] == src else None
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(getattr(self, "out", "") or "")):
+            if len(r) >= 9:
+                rows.append([x.strip() for x in r])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the CPU baseline: the fp64 oracle on a bounded sample of the workload
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, inputs, rows_per_head):
+    """Rows of the workload whose whole forward + backward share the oracle
+    computes: O, LSE, dQ for the row and its contributions to dK and dV."""
+    from exact_attention_93_gb300 import workloads as W
+    rows = []
+    flops = 0.0
+    for h in range(w.H):
+        r = W.sampled_rows(w, 0, h)
+        r = r[:: max(1, len(r) // rows_per_head)][:rows_per_head]
+        rows.append(r)
+        vis = (r + 1) if w.causal else [w.N] * len(r)
+        flops += sum(14.0 * float(v) * w.D for v in vis)  # 4 fwd + 10 bwd per key per dim
+    return rows, flops
+
+
+def time_oracle(w, inputs, rows_per_head):
+    import oracle
+    oracle.build()
+    rows, flops = oracle_sample(w, inputs, rows_per_head)
+    t0 = time.perf_counter()
+    for h in range(w.H):
+        oracle.attention_head(inputs["q"][0, h], inputs["k"][0, h], inputs["v"][0, h], w.scale,
+                              w.causal, dout=inputs["do"][0, h], rows=rows[h],
+                              kv_range=(0, w.N))
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, sum(len(r) for r in rows), oracle.threads()
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from exact_attention_93_gb300 import workloads as W
+    inputs = W.make_inputs(w)
+    rows_per_head = 8
+    for _ in range(args.warmup):
+        time_oracle(w, inputs, 2)
+    vals, secs = [], 0.0
+    cores = 1
+    for _ in range(args.steps):
+        v, dt, nrows, cores = time_oracle(w, inputs, rows_per_head)
+        vals.append(v)
+        secs += dt
+    value = statistics.mean(vals)
+    sample = (f"{rows_per_head} query rows per head x {w.H} heads of {w.describe()} "
+              f"(forward and full backward share of each row), fp64")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * secs / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe() + " fwd+bwd", "parallelism": "none (host cores)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+
+    from exact_attention_93_gb300 import fattn, workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fattn.load()
+
+    inputs = W.make_inputs(w)  # every rank runs the same replica
+    dev = torch.device("cuda", local)
+    g = {k: v.to(dev) for k, v in inputs.items()}
+    B, H, N, D = w.B, w.H, w.N, w.D
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+    det = bool(args.deterministic)
+    ws = fattn.alloc_workspace(B, H, N, D, det, dev)
+    stream = torch.cuda.current_stream()
+
+    names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq" if det else "bwd_dq_convert"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fattn.fa_fwd(g["q"], g["k"], g["v"], o, lse, w.scale, w.causal)
+        if ev is not None:
+            ev[1].record(stream)
+        fattn.fa_bwd_preprocess(o, g["do"], lse, det, ws)
+        if ev is not None:
+            ev[2].record(stream)
+        fattn.fa_bwd_dkdv(g["q"], g["k"], g["v"], g["do"], dk, dv, w.scale, w.causal, det, ws)
+        if ev is not None:
+            ev[3].record(stream)
+        if det:
+            fattn.fa_bwd_dq(g["q"], g["k"], g["v"], g["do"], dq, w.scale, w.causal, ws)
+        else:
+            fattn.fa_bwd_dq_convert(dq, w.scale, ws)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(args.steps):
+            step(events[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    per_kernel = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in events)
+                  for i, n in enumerate(names)}
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    ms_step = total_ms / args.steps
+    fwd_f, bwd_f = w.fwd_flops(), w.bwd_flops()
+    bwd_alg = bwd_f  # the deterministic pass's recomputation of S and dP is not credited
+    value = world * (fwd_f + bwd_alg) / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    peak_sust = pk["sustained"]
+    fwd_tf = fwd_f / (per_kernel["fwd"] * 1e-3) / 1e12
+    bwd_ms = sum(per_kernel[n] for n in names[1:])
+    bwd_tf = bwd_alg / (bwd_ms * 1e-3) / 1e12
+
+    # dominant kernel: the largest share of the step
+    dom = max(per_kernel, key=per_kernel.get)
+    # contraction FLOPs each tile kernel performs per launch (each N x N x D
+    # contraction is 2*N^2*D per head, halved under the causal mask):
+    #   fwd: S, PV (2);  dkdv atomic: S^T, dP^T, dV, dK, dQ (5);  dkdv
+    #   deterministic: the first four (4);  dq: S, dP, dQ (3)
+    dom_flops = {"fwd": fwd_f, "bwd_dkdv": (0.8 if det else 1.0) * bwd_f,
+                 "bwd_dq": 0.6 * bwd_f}.get(dom)
+    if dom_flops is not None:
+        achieved = dom_flops / (per_kernel[dom] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sust,
+                    "unit": "TFLOP/s", "frac": achieved / peak_sust,
+                    "peak_source": f"{pk['source']} bf16 sustained",
+                    "traffic": recorded_traffic(dom, w.name)}
+    else:  # an elementwise kernel dominating would be HBM bound
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm"],
+                    "unit": "GB/s", "frac": None, "traffic": None}
+
+    # end to end through the C ABI with host buffers: H2D inputs, step, D2H results
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in inputs.items()}
+        outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k2 in pin:
+                g[k2].copy_(pin[k2], non_blocking=True)
+            step()
+            for k2 in outs:
+                host_out[k2].copy_(outs[k2], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s2.elapsed_time(e2) / args.steps
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * (fwd_f + bwd_alg) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # the long-context forward-only workload, reported beside the step
+    extra = {}
+    if rank == 0 and w.name == "long64k_causal" and not args.no_extra:
+        w2 = W.WORKLOADS["long4k_fwd"]
+        i2 = {k: v.to(dev) for k, v in W.make_inputs(w2).items()}
+        o2 = torch.empty_like(i2["q"])
+        l2 = torch.empty(w2.B, w2.H, w2.N, dtype=torch.float32, device=dev)
+        for _ in range(5):
+            fattn.fa_fwd(i2["q"], i2["k"], i2["v"], o2, l2, w2.scale, w2.causal)
+        torch.cuda.synchronize()
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        s3.record(stream)
+        for _ in range(reps):
+            fattn.fa_fwd(i2["q"], i2["k"], i2["v"], o2, l2, w2.scale, w2.causal)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        ms2 = s3.elapsed_time(e3) / reps
+        tf2 = w2.fwd_flops() / (ms2 * 1e-3) / 1e12
+        extra[w2.describe() + " fwd"] = {"tflops": tf2, "ms": ms2,
+                                         "frac_of_burst_peak": tf2 / pk["burst"],
+                                         "note": "back-to-back launches; inputs 16.8 MB each fit in L2"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, nrows, cores = time_oracle(w, inputs, 64)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{nrows} query rows of {w.describe()} ({nrows // w.H} per head), "
+                         f"each row's whole forward and backward share, fp64, {dt:.1f} s"}
+
+    launches = len(names) * args.steps  # one kernel per entry-point call
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.describe()} fwd+bwd "
+                                   f"({'deterministic two-pass dQ' if det else 'atomic dQ'})",
+                       "B": B, "H": H, "N": N, "D": D, "causal": w.causal,
+                       "l2": "inputs larger than L2 (each input tensor "
+                             f"{B * H * N * D * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "frac_of_peak": {"fwd+bwd": value / world / peak_sust, "fwd": fwd_tf / peak_sust,
+                             "peak": peak_sust, "peak_source": f"{pk['source']} bf16 sustained"},
+            "kernel_ms": per_kernel,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from exact_attention_93_gb300 import workloads as W
+    if args.workload.startswith("custom:"):
+        B, H, N, D, dt, c = args.workload.split(":", 1)[1].split(",")
+        w = W.custom(int(B), int(H), int(N), int(D), dtype=dt, causal=c in ("1", "causal"),
+                     seed=4)
+    else:
+        w = W.WORKLOADS[args.workload]
+    if not w.backward:
+        raise SystemExit(f"workload {args.workload} has no backward; pick one that does")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

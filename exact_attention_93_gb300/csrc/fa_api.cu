@@ -1,0 +1,291 @@
+// fa_api.cu -- the C ABI of libfattn (declared in include/fattn.h): argument
+// checks, TMA descriptor set-up, workspace layout and kernel launches.  No
+// attention arithmetic lives here.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fattn.h"
+#include "fa_internal.h"
+#include "host_tmap.hpp"
+
+namespace fa {
+namespace {
+
+__device__ uint32_t g_error_word;  // written by bounded waits that run out
+
+constexpr int kMaxDevices = 64;
+
+uint32_t* error_word_ptr() {
+  static uint32_t* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Shape {
+  int B, H, N, D;
+  long long BH() const { return static_cast<long long>(B) * H; }
+  int Npad() const { return (N + kTile - 1) / kTile * kTile; }
+};
+
+// Sizes only; pointers are checked by each entry point.
+fa_status check_shape(const Shape& s, int dtype) {
+  if (s.B < 1 || s.H < 1 || s.N < 1) return FA_ERR_INVALID_ARG;
+  if (s.D != 64 && s.D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
+  if (s.BH() > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (static_cast<double>(s.BH()) * s.N * s.D >= 1099511627776.0) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) { return std::isfinite(scale) ? FA_OK : FA_ERR_INVALID_ARG; }
+
+struct WsLayout {
+  size_t lse2 = 0, di = 0, dq = 0, total = 0;
+};
+
+WsLayout ws_layout(const Shape& s, int deterministic) {
+  WsLayout w;
+  const size_t rows = static_cast<size_t>(s.BH()) * s.Npad();
+  w.lse2 = 0;
+  w.di = round256(rows * 4);
+  w.dq = w.di + round256(rows * 4);
+  w.total = w.dq + (deterministic ? 0 : round256(static_cast<size_t>(s.BH()) * s.N * s.D * 4));
+  return w;
+}
+
+fa_status check_ws(const Shape& s, int deterministic, const void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (bytes < ws_layout(s, deterministic).total) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype) {
+  return make_tmap_3d(m, base,
+                      dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      2, static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.N),
+                      static_cast<uint64_t>(s.BH()), static_cast<uint64_t>(s.D),
+                      static_cast<uint64_t>(s.N) * s.D, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Everything the dK/dV and dQ kernels share.
+fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void* v,
+                          const void* dO, void* dq, void* dk, void* dv, const Shape& s, float scale,
+                          int causal, int dtype, int deterministic, void* ws) {
+  *a = BwdLaunch{};
+  if (!tile_map(&a->map_q, q, s, dtype) || !tile_map(&a->map_k, k, s, dtype) ||
+      !tile_map(&a->map_v, v, s, dtype) || !tile_map(&a->map_do, dO, s, dtype))
+    return FA_ERR_CUDA;
+  if (dq && !tile_map(&a->map_dq, dq, s, dtype)) return FA_ERR_CUDA;
+  if (dk && !tile_map(&a->map_dk, dk, s, dtype)) return FA_ERR_CUDA;
+  if (dv && !tile_map(&a->map_dv, dv, s, dtype)) return FA_ERR_CUDA;
+  const WsLayout w = ws_layout(s, deterministic);
+  auto* base = static_cast<uint8_t*>(ws);
+  a->lse = reinterpret_cast<const float*>(base + w.lse2);
+  a->di = reinterpret_cast<const float*>(base + w.di);
+  a->dq_accum = deterministic ? nullptr : reinterpret_cast<float*>(base + w.dq);
+  a->N = s.N;
+  a->BH = static_cast<int>(s.BH());
+  a->D = s.D;
+  a->scale = scale;
+  a->scale_log2 = scale * kLog2e;
+  a->causal = causal ? 1 : 0;
+  a->bf16 = dtype == FA_BF16 ? 1 : 0;
+  a->err = error_word_ptr();
+  return a->err ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_abi_version(void) { return 1; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int D, float scale, int causal, fa_dtype dtype, void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  FwdLaunch a{};
+  if (!tile_map(&a.map_q, q, s, dtype) || !tile_map(&a.map_k, k, s, dtype) ||
+      !tile_map(&a.map_v, v, s, dtype) || !tile_map(&a.map_o, o, s, dtype))
+    return FA_ERR_CUDA;
+  a.lse = lse;
+  a.N = N;
+  a.BH = static_cast<int>(s.BH());
+  a.D = D;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.bf16 = dtype == FA_BF16 ? 1 : 0;
+  a.err = error_word_ptr();
+  if (!a.err) return FA_ERR_CUDA;
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic) {
+  const Shape s{B, H, N, D};
+  if (check_shape(s, FA_BF16) != FA_OK) return 0;
+  return ws_layout(s, deterministic).total;
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int H, int N,
+                            int D, fa_dtype dtype, int deterministic, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
+  const WsLayout w = ws_layout(s, deterministic);
+  auto* base = static_cast<uint8_t*>(workspace);
+  return from_cuda(launch_bwd_preprocess(
+      o, dO, lse, reinterpret_cast<float*>(base + w.lse2), reinterpret_cast<float*>(base + w.di),
+      deterministic ? nullptr : reinterpret_cast<float*>(base + w.dq), N, s.BH(), D,
+      dtype == FA_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                      void* dv, int B, int H, int N, int D, float scale, int causal,
+                      fa_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
+  BwdLaunch a;
+  if ((st = make_bwd_launch(&a, q, k, v, dO, nullptr, dk, dv, s, scale, causal, dtype,
+                            deterministic, workspace)) != FA_OK)
+    return st;
+  return from_cuda(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B,
+                    int H, int N, int D, float scale, int causal, fa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq))
+    return FA_ERR_INVALID_ARG;
+  if ((st = check_ws(s, 1, workspace, workspace_bytes)) != FA_OK) return st;
+  BwdLaunch a;
+  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, nullptr, nullptr, s, scale, causal, dtype, 1,
+                            workspace)) != FA_OK)
+    return st;
+  return from_cuda(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int D, float scale, fa_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(dq)) return FA_ERR_INVALID_ARG;
+  if ((st = check_ws(s, 0, workspace, workspace_bytes)) != FA_OK) return st;
+  const WsLayout w = ws_layout(s, 0);
+  const float* acc = reinterpret_cast<const float*>(static_cast<uint8_t*>(workspace) + w.dq);
+  return from_cuda(launch_dq_convert(acc, dq, s.BH() * s.N * s.D, scale, dtype == FA_BF16,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                 float scale, int causal, fa_dtype dtype, int deterministic, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  const Shape s{B, H, N, D};
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
+  // Build every descriptor before enqueueing anything.
+  BwdLaunch a;
+  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, dk, dv, s, scale, causal, dtype, deterministic,
+                            workspace)) != FA_OK)
+    return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const WsLayout w = ws_layout(s, deterministic);
+  auto* base = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_bwd_preprocess(
+      o, dO, lse, reinterpret_cast<float*>(base + w.lse2), reinterpret_cast<float*>(base + w.di),
+      a.dq_accum, N, s.BH(), D, dtype == FA_BF16, cs);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if ((e = launch_bwd_dkdv(a, cs)) != cudaSuccess) return FA_ERR_CUDA;
+  if (deterministic) return from_cuda(launch_bwd_dq(a, cs));
+  return from_cuda(
+      launch_dq_convert(a.dq_accum, dq, s.BH() * s.N * s.D, scale, dtype == FA_BF16, cs));
+}
+
+fa_status fa_device_error(void* stream, int* code) {
+  if (!code) return FA_ERR_INVALID_ARG;
+  uint32_t* p = error_word_ptr();
+  if (!p) return FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  *code = v == 0 ? FA_OK : FA_ERR_TIMEOUT;
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 2000000) return FA_ERR_INVALID_ARG;
+  uint32_t* p = error_word_ptr();
+  if (!p) return FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (launch_wait_selftest(p, static_cast<uint64_t>(limit_us) * 1000ull, cs) != cudaSuccess)
+    return FA_ERR_CUDA;
+  int code = FA_OK;
+  fa_status st = fa_device_error(stream, &code);
+  if (st != FA_OK) return st;
+  return static_cast<fa_status>(code);
+}
+
+}  // extern "C"

@@ -1,0 +1,735 @@
+// fa_bwd.cu -- exact attention backward for sm_103a: recompute P from Q, K
+// and the forward's log-sum-exp instead of storing it ("FlashAttention from
+// scratch" walkthrough, l189.com, sec. 3.3; "FlashAttention 深入", backward
+// recomputation).
+//
+//   preprocess  Di = rowsum(dO * O) (fp32), the full-row statistic of the
+//               softmax Jacobian; LSE rescaled to log2 units; both padded to
+//               whole 128-row tiles (+inf / 0) so the tile kernels can copy
+//               them with one bulk copy.  Also zeroes the fp32 dQ accumulator.
+//   dkdv        one CTA per 128-key tile, looping over 128-query tiles:
+//                 S^T  = K Q^T            (TMEM)      P^T = exp2(S^T*c - lse2)
+//                 dP^T = V dO^T           (TMEM)      dS^T = P^T (dP^T - Di)
+//                 dV  += P^T dO           (A = P^T written back into TMEM)
+//                 dK  += dS^T Q           (A = dS^T in swizzled smem)
+//                 dQ_i = dS K             (atomic mode; A = dS^T read MN-major)
+//               dQ rows are added to an fp32 accumulator with vector atomics.
+//   dq          deterministic mode: one CTA per 128-query tile looping over
+//               key tiles, dQ accumulated in TMEM, no atomics.
+//   dq_convert  dQ = scale * accumulator, rounded to the input type.
+//
+// Warp roles in the tile kernels (192 threads): warps 0-3 elementwise work,
+// one TMEM lane (one tile row) per thread; warp 4 TMA producer; warp 5 MMA
+// issuer.  Every wait is bounded.
+#include <climits>
+
+#include "fa_internal.h"
+#include "sm103_primitives.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort_flag) {
+  bool ok = mbar_wait(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// Write 32 consecutive 16-bit values (16 packed words) of tile row r,
+// columns [32*c32, 32*c32 + 32), into a 128-byte-swizzled tile made of
+// 64-column blocks of 128 rows.
+__device__ __forceinline__ void store_row_chunk_sw128(uint8_t* tile, int r, int c32,
+                                                      const uint32_t (&pk)[16]) {
+  uint8_t* row = tile + (c32 >> 1) * (kTile * 128) + r * 128;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const int cc = (c32 & 1) * 4 + ch;
+    *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) * 16)) =
+        make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// preprocess
+// ---------------------------------------------------------------------------
+// One group of D/8 threads per row; each thread handles 8 columns.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __restrict__ o,
+                                                             const uint16_t* __restrict__ dO,
+                                                             const float* __restrict__ lse,
+                                                             float* __restrict__ lse2,
+                                                             float* __restrict__ di,
+                                                             float* __restrict__ dq_accum, int N,
+                                                             int Npad, long long BH) {
+  constexpr int G = D / 8;  // threads per row
+  const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long prow = gtid / G;  // padded row index over BH * Npad
+  const int part = static_cast<int>(gtid % G);
+  if (prow >= BH * Npad) return;
+  const long long bh = prow / Npad;
+  const int n = static_cast<int>(prow % Npad);
+  float acc = 0.f;
+  if (n < N) {
+    const long long row = bh * N + n;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + part * 8);
+    const uint32_t* aa = reinterpret_cast<const uint32_t*>(&a);
+    const uint32_t* bb = reinterpret_cast<const uint32_t*>(&b);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 x = unpack2<kBf16>(aa[t]), y = unpack2<kBf16>(bb[t]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+    if (dq_accum) {
+      float4* z = reinterpret_cast<float4*>(dq_accum + row * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+  if (part == 0) {
+    di[prow] = acc;
+    lse2[prow] = (n < N) ? lse[bh * N + n] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV (and atomic dQ)
+// ---------------------------------------------------------------------------
+template <int D>
+struct DkdvSmem {
+  static constexpr int kBlocks = D / 64;
+  static constexpr int kBlockBytes = kTile * 128;
+  static constexpr int kTileBytes = kBlocks * kBlockBytes;
+  alignas(1024) uint8_t k[kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t q[kTileBytes];   // reused for the dK output tile
+  alignas(1024) uint8_t dO[kTileBytes];  // reused for the dV output tile
+  alignas(1024) uint8_t dst[2 * kBlockBytes];  // dS^T: 128 keys x 128 queries
+  alignas(16) float lse2[kTile];
+  alignas(16) float di[kTile];
+  uint64_t kv_full, qdo_full, qdo_empty, s_full, p_full, mma_done, tmem_free, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, bool kBf16, bool kCausal, bool kAtomicDq>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdLaunch p) {
+  using Smem = DkdvSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = (p.N + kTile - 1) / kTile;
+  const int Npad = n_tiles * kTile;
+  int kt, bh;
+  if (kCausal) {  // key tiles near the start see the most queries: first
+    kt = static_cast<int>(blockIdx.x / p.BH);
+    bh = static_cast<int>(blockIdx.x % p.BH);
+  } else {
+    kt = static_cast<int>(blockIdx.x % n_tiles);
+    bh = static_cast<int>(blockIdx.x / n_tiles);
+  }
+  const int k0 = kt * kTile;
+  const int it_begin = kCausal ? kt : 0;
+  const int n_it = n_tiles - it_begin;
+
+  if (tid == 0) {
+    mbar_init(&s.kv_full, 1);
+    mbar_init(&s.qdo_full, 1);
+    mbar_init(&s.qdo_empty, 1);
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.mma_done, 1);
+    mbar_init(&s.tmem_free, 128);
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + D;
+  const uint32_t tdQ = tbase;  // aliases S^T once it has been consumed
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.kv_full, 2 * Smem::kTileBytes);
+      for (int kb = 0; kb < Smem::kBlocks; ++kb) {
+        tma_load_3d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.kv_full, kb * 64, k0, bh);
+        tma_load_3d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.kv_full, kb * 64, k0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int q0 = (it_begin + it) * kTile;
+        if (it >= 1 && !mbar_wait(&s.qdo_empty, (it - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes + 2 * kTile * 4);
+        for (int kb = 0; kb < Smem::kBlocks; ++kb) {
+          tma_load_3d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, bh);
+          tma_load_3d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, bh);
+        }
+        const long long off = static_cast<long long>(bh) * Npad + q0;
+        bulk_load(s.lse2, p.lse + off, kTile * 4, &s.qdo_full);
+        bulk_load(s.di, p.di + off, kTile * 4, &s.qdo_full);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        int zero = 0;
+        mbar_wait(&s.kv_full, 0, p.err, &zero, 100000000ull);
+        if (issued > 0) mbar_wait(&s.qdo_full, (issued - 1) & 1, p.err, &zero, 100000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ab = kBf16 ? 1u : 0u;
+      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);   // K-major A and B
+      constexpr uint32_t idKM = idesc_f16(128, D, ab, 0, 1);    // A K-major, B MN-major
+      constexpr uint32_t idMM = idesc_f16(128, D, ab, 1, 1);    // both MN-major
+      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
+      const uint32_t dst_addr = smem_u32(s.dst);
+      bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
+      for (int it = 0; ok && it < n_it; ++it) {
+        if (!mbar_wait(&s.qdo_full, it & 1, p.err, abort_flag)) break;
+        if (kAtomicDq && it >= 1 && !mbar_wait(&s.tmem_free, (it - 1) & 1, p.err, abort_flag))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tS, smem_desc_sw128(k_addr + off, 16, 1024),
+                    smem_desc_sw128(q_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tdP, smem_desc_sw128(v_addr + off, 16, 1024),
+                    smem_desc_sw128(do_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s.s_full);
+        if (!mbar_wait(&s.p_full, it & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        // dV += P^T dO : A = P^T in TMEM (16-bit pairs over S^T columns [0, 64))
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ts(tdV, tS + kk * 8, smem_desc_sw128(do_addr + kk * 16 * 128, Smem::kBlockBytes, 1024),
+                    idKM, (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q : A = dS^T in smem, K-major over queries
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tdK, smem_desc_sw128(dst_addr + aoff, 16, 1024),
+                    smem_desc_sw128(q_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idKM,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (kAtomicDq) {
+          // dQ_i = dS K : A = dS (queries x keys) read MN-major from dS^T
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            tc_mma_ss(tdQ, smem_desc_sw128(dst_addr + kk * 16 * 128, Smem::kBlockBytes, 1024),
+                      smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idMM,
+                      kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s.mma_done);
+        tc_commit(&s.qdo_empty);
+      }
+      tc_commit(&s.drain);
+      int zero = 0;
+      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int r = tid;  // key row within the tile (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int q0 = (it_begin + it) * kTile;
+      if (!warp_wait(&s.s_full, it & 1, p.err, abort_flag) ||
+          !warp_wait(&s.qdo_full, it & 1, p.err, abort_flag)) {  // lse2 / Di of this tile
+        ok = false;
+        break;
+      }
+      // dS^T smem of the previous tile must have been consumed
+      if (!kAtomicDq && it >= 1 && !warp_wait(&s.mma_done, (it - 1) & 1, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = kCausal && (q0 == k0);
+#pragma unroll 1
+      for (int c = 0; c < kTile / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + lane_off + c * 32, sr);
+        tmem_ld32(tdP + lane_off + c * 32, dr);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[c * 32 + t]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[c * 32 + t]);
+          const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = c * 32 + t + e;  // query index within the tile
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
+            if (diag && col < r) pe = 0.f;
+            pv[e] = pe;
+            dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
+          }
+          pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
+          pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
+          dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
+          dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
+        }
+        // P^T over columns already read: [16c, 16c + 16) <= [32c, 32c + 32)
+        tmem_st16(tS + lane_off + c * 16, pk);
+        store_row_chunk_sw128(s.dst, r, c, dk);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+
+      if (kAtomicDq) {
+        if (!warp_wait(&s.mma_done, it & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int qrow = q0 + r;  // dQ tile rows are queries
+        float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + qrow) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t g[32];
+          tmem_ld32(tdQ + lane_off + c * 32, g);
+          tmem_ld_wait();
+          if (qrow < p.N) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 4)
+              red_add_v4(dst + c * 32 + t, __uint_as_float(g[t]), __uint_as_float(g[t + 1]),
+                         __uint_as_float(g[t + 2]), __uint_as_float(g[t + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s.tmem_free);
+      }
+    }
+
+    // ---------------------------------------------------------- epilogue
+    bool done = ok;
+    if (ok && !kAtomicDq) done = warp_wait(&s.mma_done, (n_it - 1) & 1, p.err, abort_flag);
+    if (named_bar_and(1, 128, done)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tdV + lane_off + c * 32, a);
+        tmem_ld32(tdK + lane_off + c * 32, b);
+        tmem_ld_wait();
+        uint32_t pa[16], pb[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          pa[t] = pack2<kBf16>(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
+          pb[t] = pack2<kBf16>(__uint_as_float(b[2 * t]) * p.scale,
+                               __uint_as_float(b[2 * t + 1]) * p.scale);
+        }
+        store_row_chunk_sw128(s.dO, r, c, pa);
+        store_row_chunk_sw128(s.q, r, c, pb);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        for (int kb = 0; kb < Smem::kBlocks; ++kb) {
+          tma_store_3d(&p.map_dv, s.dO + kb * Smem::kBlockBytes, kb * 64, k0, bh);
+          tma_store_3d(&p.map_dk, s.q + kb * Smem::kBlockBytes, kb * 64, k0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// deterministic dQ
+// ---------------------------------------------------------------------------
+template <int D>
+struct DqSmem {
+  static constexpr int kBlocks = D / 64;
+  static constexpr int kBlockBytes = kTile * 128;
+  static constexpr int kTileBytes = kBlocks * kBlockBytes;
+  alignas(1024) uint8_t q[kTileBytes];  // reused for the dQ output tile
+  alignas(1024) uint8_t dO[kTileBytes];
+  alignas(1024) uint8_t k[kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t ds[2 * kBlockBytes];  // dS: 128 queries x 128 keys
+  uint64_t qdo_full, k_full, k_empty, v_full, v_empty, s_full, p_full, mma_done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdLaunch p) {
+  using Smem = DqSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = (p.N + kTile - 1) / kTile;
+  const int Npad = n_tiles * kTile;
+  int qt, bh;
+  if (kCausal) {
+    qt = n_tiles - 1 - static_cast<int>(blockIdx.x / p.BH);
+    bh = static_cast<int>(blockIdx.x % p.BH);
+  } else {
+    qt = static_cast<int>(blockIdx.x % n_tiles);
+    bh = static_cast<int>(blockIdx.x / n_tiles);
+  }
+  const int q0 = qt * kTile;
+  const int n_kv = kCausal ? qt + 1 : n_tiles;
+
+  if (tid == 0) {
+    mbar_init(&s.qdo_full, 1);
+    mbar_init(&s.k_full, 1);
+    mbar_init(&s.k_empty, 1);
+    mbar_init(&s.v_full, 1);
+    mbar_init(&s.v_empty, 1);
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.mma_done, 1);
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  const uint32_t tS = tbase, tdP = tbase + 128, tdQ = tbase + 256;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes);
+      for (int kb = 0; kb < Smem::kBlocks; ++kb) {
+        tma_load_3d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, bh);
+        tma_load_3d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        if (j >= 1 && !mbar_wait(&s.k_empty, (j - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(&s.k_full, Smem::kTileBytes);
+        for (int kb = 0; kb < Smem::kBlocks; ++kb)
+          tma_load_3d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, j * kTile, bh);
+        issued = 2 * j + 1;
+        if (j >= 1 && !mbar_wait(&s.v_empty, (j - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(&s.v_full, Smem::kTileBytes);
+        for (int kb = 0; kb < Smem::kBlocks; ++kb)
+          tma_load_3d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, j * kTile, bh);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        int zero = 0;
+        mbar_wait(&s.qdo_full, 0, p.err, &zero, 100000000ull);
+        if (issued >= 1) mbar_wait(&s.k_full, ((issued - 1) >> 1) & 1, p.err, &zero, 100000000ull);
+        if (issued >= 2) mbar_wait(&s.v_full, ((issued - 2) >> 1) & 1, p.err, &zero, 100000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t ab = kBf16 ? 1u : 0u;
+      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
+      constexpr uint32_t idKM = idesc_f16(128, D, ab, 0, 1);
+      const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
+      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v), ds_addr = smem_u32(s.ds);
+      bool ok = mbar_wait(&s.qdo_full, 0, p.err, abort_flag);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (!mbar_wait(&s.k_full, j & 1, p.err, abort_flag)) break;
+        if (!mbar_wait(&s.v_full, j & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tS, smem_desc_sw128(q_addr + off, 16, 1024),
+                    smem_desc_sw128(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tdP, smem_desc_sw128(do_addr + off, 16, 1024),
+                    smem_desc_sw128(v_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s.s_full);
+        tc_commit(&s.v_empty);
+        if (!mbar_wait(&s.p_full, j & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        // dQ += dS K : A = dS in smem K-major over keys, B = K MN-major
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+          tc_mma_ss(tdQ, smem_desc_sw128(ds_addr + aoff, 16, 1024),
+                    smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idKM,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&s.mma_done);
+        tc_commit(&s.k_empty);
+      }
+      tc_commit(&s.drain);
+      int zero = 0;
+      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+    }
+  } else {
+    const int r = tid;  // query row within the tile
+    const int i = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const long long srow = static_cast<long long>(bh) * Npad + i;
+    const float lse2 = p.lse[srow];
+    const float dii = p.di[srow];
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!warp_wait(&s.s_full, j & 1, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (j >= 1 && !warp_wait(&s.mma_done, (j - 1) & 1, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = j * kTile;
+      const bool diag = kCausal && (k0 == q0);
+#pragma unroll 1
+      for (int c = 0; c < kTile / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + lane_off + c * 32, sr);
+        tmem_ld32(tdP + lane_off + c * 32, dr);
+        tmem_ld_wait();
+        uint32_t dk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float d2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + t + e;  // key index within the tile
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -lse2));
+            if (diag && col > r) pe = 0.f;
+            d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
+          }
+          dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
+        }
+        store_row_chunk_sw128(s.ds, r, c, dk);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+    }
+    const bool mine = ok && warp_wait(&s.mma_done, (n_kv - 1) & 1, p.err, abort_flag);
+    if (named_bar_and(1, 128, mine)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t g[32];
+        tmem_ld32(tdQ + lane_off + c * 32, g);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack2<kBf16>(__uint_as_float(g[2 * t]) * p.scale,
+                               __uint_as_float(g[2 * t + 1]) * p.scale);
+        store_row_chunk_sw128(s.q, r, c, pk);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        for (int kb = 0; kb < Smem::kBlocks; ++kb)
+          tma_store_3d(&p.map_dq, s.q + kb * Smem::kBlockBytes, kb * 64, q0, bh);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ convert
+// ---------------------------------------------------------------------------
+template <bool kBf16>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         uint16_t* __restrict__ dq,
+                                                         long long n8, float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
+       t += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+    uint4 o;
+    o.x = pack2<kBf16>(a.x * scale, a.y * scale);
+    o.y = pack2<kBf16>(a.z * scale, a.w * scale);
+    o.z = pack2<kBf16>(b.x * scale, b.y * scale);
+    o.w = pack2<kBf16>(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[t] = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self test: one barrier nobody signals
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, err, &abort_flag, limit_ns);
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes, bool& configured) {
+  if (configured) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) configured = true;
+  return e;
+}
+
+template <int D, bool kBf16, bool kCausal, bool kAtomic>
+cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
+  auto kern = bwd_dkdv_kernel<D, kBf16, kCausal, kAtomic>;
+  const int smem = static_cast<int>(sizeof(DkdvSmem<D>)) + 1024;
+  static bool configured = false;
+  cudaError_t e = set_smem(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
+  auto kern = bwd_dq_kernel<D, kBf16, kCausal>;
+  const int smem = static_cast<int>(sizeof(DqSmem<D>)) + 1024;
+  static bool configured = false;
+  cudaError_t e = set_smem(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
+  const bool atomic = a.dq_accum != nullptr;
+  if (a.causal)
+    return atomic ? launch_dkdv_t<D, kBf16, true, true>(a, st) : launch_dkdv_t<D, kBf16, true, false>(a, st);
+  return atomic ? launch_dkdv_t<D, kBf16, false, true>(a, st) : launch_dkdv_t<D, kBf16, false, false>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* lse2,
+                                  float* di, float* dq_accum, int N, long long BH, int D, int bf16,
+                                  cudaStream_t st) {
+  const int Npad = (N + kTile - 1) / kTile * kTile;
+  const long long threads = BH * Npad * (D / 8);
+  const long long blocks = (threads + 255) / 256;
+  if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
+  const auto* o16 = static_cast<const uint16_t*>(o);
+  const auto* d16 = static_cast<const uint16_t*>(dO);
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (D == 64) {
+    if (bf16) bwd_preprocess_kernel<64, true><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+    else bwd_preprocess_kernel<64, false><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+  } else {
+    if (bf16) bwd_preprocess_kernel<128, true><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+    else bwd_preprocess_kernel<128, false><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t st) {
+  if (a.D == 64) return a.bf16 ? launch_dkdv_d<64, true>(a, st) : launch_dkdv_d<64, false>(a, st);
+  return a.bf16 ? launch_dkdv_d<128, true>(a, st) : launch_dkdv_d<128, false>(a, st);
+}
+
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t st) {
+  if (a.D == 64) {
+    if (a.bf16) return a.causal ? launch_dq_t<64, true, true>(a, st) : launch_dq_t<64, true, false>(a, st);
+    return a.causal ? launch_dq_t<64, false, true>(a, st) : launch_dq_t<64, false, false>(a, st);
+  }
+  if (a.bf16) return a.causal ? launch_dq_t<128, true, true>(a, st) : launch_dq_t<128, true, false>(a, st);
+  return a.causal ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
+}
+
+cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale, int bf16,
+                              cudaStream_t st) {
+  const long long n8 = n / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  if (bf16)
+    dq_convert_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<uint16_t*>(dq), n8, scale);
+  else
+    dq_convert_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<uint16_t*>(dq), n8, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,45 @@
+// fa_internal.h -- launch interface between the C ABI (fa_api.cu) and the
+// kernel translation units.  Host-side only; no device code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fa {
+
+constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
+
+struct FwdLaunch {
+  CUtensorMap map_q, map_k, map_v, map_o;  // [BH][N][D], box 64 x 128, 128B swizzle
+  float* lse;                               // [BH][N]
+  int N, BH, D;
+  float scale_log2;                         // scale * log2(e)
+  int causal, bf16;
+  uint32_t* err;
+};
+
+struct BwdLaunch {
+  CUtensorMap map_q, map_k, map_v, map_do;  // [BH][N][D], box 64 x 128
+  CUtensorMap map_dq, map_dk, map_dv;       // outputs, same geometry
+  const float* lse;                         // [BH][Npad] LSE * log2(e), +inf padding
+  const float* di;                          // [BH][Npad] rowsum(dO * O), 0 padding
+  float* dq_accum;                          // [BH][N][D] or nullptr
+  int N, BH, D;
+  float scale, scale_log2;
+  int causal, bf16;
+  uint32_t* err;
+};
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* lse2,
+                                  float* di, float* dq_accum, int N, long long BH, int D, int bf16,
+                                  cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);
+cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale, int bf16,
+                              cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace fa

@@ -17,9 +17,10 @@ Q, K, V and then dO are drawn in that order, each as
 (round to nearest even).  The fp16 workload scales dO by 0.1 (standard
 deviation 0.1) before rounding.  Workloads without a backward draw Q, K, V only.
 
-Query rows checked on large shapes: per (b, h), 256 distinct rows drawn by
-``numpy.random.default_rng(seed * 1_000_003 + b * H + h).choice(N, 256,
-replace=False)``, plus rows 0 and N - 1, sorted.  For causal workloads the
+Query rows checked on large shapes: per (b, h), 256 distinct interior rows
+drawn by ``numpy.random.default_rng(seed * 1_000_003 + b * H + h).choice(
+arange(1, N - 1), 256, replace=False)``, plus rows 0 and N - 1, sorted (258
+rows in all).  For causal workloads the
 last key tile's gradient is checked too, which needs the last ``tail`` query
 rows in full (see ``tail_rows``).
 """
@@ -108,11 +109,11 @@ def custom(B, H, N, D, dtype="bf16", causal=False, seed=0, backward=True,
 
 def sampled_rows(w: Workload, b: int, h: int, count: int = 256) -> np.ndarray:
     """Sorted distinct query rows checked against the oracle for (b, h)."""
-    if not w.sampled or w.N <= count:
+    if not w.sampled or w.N <= count + 2:
         return np.arange(w.N, dtype=np.int64)
     rng = np.random.default_rng(w.seed * 1_000_003 + b * w.H + h)
-    r = rng.choice(w.N, count, replace=False)
-    r = np.union1d(r, np.array([0, w.N - 1]))
+    r = rng.choice(np.arange(1, w.N - 1), count, replace=False)
+    r = np.concatenate([r, np.array([0, w.N - 1])])
     return np.sort(r).astype(np.int64)
 
 

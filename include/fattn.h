@@ -1,0 +1,167 @@
+/*
+ * fattn.h -- libfattn: exact tiled attention on one sm_103a GPU (C ABI).
+ *
+ * Computes O = softmax(scale * Q K^T [+ causal mask]) V exactly, tile by tile
+ * with an online softmax, and its gradients by recomputing P from Q, K and
+ * the saved per-row log-sum-exp instead of storing the N x N matrix.
+ *
+ * Sources for what is computed (the pages this library follows):
+ *   [WALK] "FlashAttention from scratch in PyTorch" walkthrough (l189.com
+ *          news 1255901): sec. 1.1 standard attention, sec. 2.2 online
+ *          softmax, sec. 2.4 tiling loop, sec. 3.1 forward with the saved
+ *          log-sum-exp, sec. 3.3 recompute backward and softmax Jacobian,
+ *          sec. 5.2 fp32 statistics, sec. 5.3 causal mask.
+ *   [DEEP] "FlashAttention 深入" (LLM interview guide): online softmax,
+ *          backward recomputation, v2 sequence-dimension parallelism.
+ *   [API]  claire-chang.com FlashAttention introduction: the flash_attn_func
+ *          argument list (softmax_scale, causal, deterministic).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *   Layout   Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, D] arrays of
+ *            16-bit floats, D innermost ([WALK] sec. 1.1, "Q, K, V: (batch,
+ *            heads, seq_len, dim)").  LSE and Di are contiguous fp32 [B, H, N].
+ *            Q, K and V share N (self-attention).
+ *   Types    FA_BF16 or FA_FP16, the same for every 16-bit array of a call.
+ *            Accumulation and softmax statistics are fp32 ([WALK] sec. 5.2).
+ *   Shapes   B, H, N >= 1; D is 64 or 128; B * H <= 2^31 - 1 and
+ *            B * H * N * D < 2^40.
+ *   Pointers Device pointers, 16-byte aligned (TMA requirement).  The caller
+ *            owns every buffer; the library allocates no device memory.
+ *   Streams  `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *            call only enqueues work and returns; results are ready once the
+ *            stream reaches that point.
+ *   Errors   Arguments are checked before anything is enqueued.  A failed
+ *            check returns FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED and
+ *            enqueues nothing.  A failed launch returns FA_ERR_CUDA.  Kernels
+ *            bound every internal wait; a wait that runs out records
+ *            FA_ERR_TIMEOUT in a device-side error word that fa_device_error()
+ *            reads.
+ *   Threads  Calls may come from several host threads; the only shared state
+ *            is the device error word and the lazily fetched driver entry
+ *            point for building TMA descriptors.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, bad scale   */
+  FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, unknown dtype                 */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed              */
+  FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait                */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/* Version of this interface (incremented on any signature change). */
+int fa_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Forward pass ([WALK] sec. 2.4 and 3.1; [DEEP] online softmax).
+ *
+ *   o[b,h,i,:]  = sum_j P_ij V[b,h,j,:],  P = softmax_j(scale * Q_i . K_j)
+ *   lse[b,h,i]  = ln sum_j exp(scale * Q_i . K_j)   (natural log, scaled scores)
+ *
+ * With causal != 0 query i sees keys j <= i only ([WALK] sec. 5.3); tiles
+ * above the diagonal are skipped.  `scale` must be finite (the usual value is
+ * 1/sqrt(D), [API] softmax_scale default).  Writes o and lse only.
+ * Deterministic: the same inputs give bit-identical outputs.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int D, float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Workspace bytes fa_bwd needs, laid out as (each part 256-byte aligned):
+ *   lse2      fp32 [B*H][Npad]   LSE * log2(e); +inf for padding rows
+ *   di        fp32 [B*H][Npad]   Di = rowsum(dO * O); 0 for padding rows
+ *   dq_accum  fp32 [B*H][N][D]   only when deterministic == 0
+ * where Npad is N rounded up to a multiple of 128.  Returns 0 for invalid
+ * sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic);
+
+/*
+ * Backward pass ([WALK] sec. 3.3; [DEEP] backward recomputation): given the
+ * forward's o and lse and the upstream gradient dO, writes dq, dk, dv.
+ *
+ *   P_ij  = exp(scale * Q_i . K_j - lse_i)        recomputed, never stored
+ *   Di    = sum_d dO_id O_id                      (= sum_j P_ij dP_ij)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dS_ij = P_ij (dO_i . V_j - Di)
+ *   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
+ *
+ * deterministic == 0: dQ is accumulated with fp32 atomics into the workspace
+ *   and converted at the end (fast; summation order varies run to run).
+ * deterministic != 0: a second pass computes dQ one query tile at a time with
+ *   no atomics; results are bit-identical across runs ([API] deterministic).
+ * `workspace` must hold fa_bwd_workspace_size(...) bytes, 256-byte aligned;
+ * its contents on entry do not matter.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                 float scale, int causal, fa_dtype dtype, int deterministic, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
+ * The stages fa_bwd enqueues, for callers that schedule or time them
+ * separately.  fa_bwd(...) is exactly fa_bwd_preprocess, then fa_bwd_dkdv,
+ * then fa_bwd_dq_convert (deterministic == 0) or fa_bwd_dq (otherwise), all
+ * on one stream with one workspace.
+ */
+
+/* Fills lse2 and di in the workspace (and zeroes dq_accum when
+ * deterministic == 0) from o, dO and the forward's lse. */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int B, int H, int N,
+                            int D, fa_dtype dtype, int deterministic, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* One pass over key tiles, each looping over query tiles: writes dk and dv.
+ * When deterministic == 0 it also adds sum_j dS_ij K_j (without the scale
+ * factor) into the workspace's dq_accum with fp32 atomics. */
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                      void* dv, int B, int H, int N, int D, float scale, int causal,
+                      fa_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Deterministic dQ: one query tile per CTA looping over key tiles, no
+ * atomics.  Needs lse2 and di in the workspace. */
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq, int B,
+                    int H, int N, int D, float scale, int causal, fa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* dq = scale * dq_accum (the workspace of a deterministic == 0 call),
+ * rounded to dtype. */
+fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int D, float scale, fa_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits write.  *code receives FA_OK or FA_ERR_TIMEOUT.  Returns
+ * FA_ERR_CUDA if the synchronisation or the read fails.
+ */
+fa_status fa_device_error(void* stream, int* code);
+
+/*
+ * Failure-detection self test: enqueues one small kernel that waits on a
+ * barrier nothing ever signals, with a limit of `limit_us` microseconds
+ * (1 <= limit_us <= 2000000), then reads the error word as fa_device_error
+ * does.  Returns FA_ERR_TIMEOUT when the wait ran out as intended; the
+ * context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

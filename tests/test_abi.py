@@ -1,0 +1,119 @@
+"""The C ABI on the host: libfattn.so builds, loads, exports every function
+include/fattn.h declares, and rejects bad arguments before anything reaches
+CUDA.  No kernel runs here."""
+import ctypes
+import subprocess
+
+import pytest
+
+from exact_attention_93_gb300 import build, fattn
+
+NULL = None
+EXPECTED = [
+    "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert",
+    "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_device_error", "fa_fwd",
+    "fa_selftest_wait_timeout", "fa_status_string",
+]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fattn.load()
+
+
+def test_header_declares_the_expected_entry_points():
+    assert fattn.declared_symbols() == sorted(EXPECTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fattn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in fattn.declared_symbols():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_abi_version() == 1
+    names = [lib.fa_status_string(i).decode() for i in range(5)]
+    assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
+                     "FA_ERR_TIMEOUT"]
+    assert lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+
+
+FAKE = 1 << 20  # an aligned, never dereferenced address: every case below fails before use
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, D=64, scale=0.125,
+        causal=0, dtype=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, D, ctypes.c_float(scale), causal, dtype, NULL)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"q": NULL}, fattn.FA_ERR_INVALID_ARG),
+    ({"lse": NULL}, fattn.FA_ERR_INVALID_ARG),
+    ({"v": FAKE + 8}, fattn.FA_ERR_INVALID_ARG),     # not 16-byte aligned
+    ({"B": 0}, fattn.FA_ERR_INVALID_ARG),
+    ({"H": -1}, fattn.FA_ERR_INVALID_ARG),
+    ({"N": 0}, fattn.FA_ERR_INVALID_ARG),
+    ({"D": 96}, fattn.FA_ERR_UNSUPPORTED),
+    ({"D": 256}, fattn.FA_ERR_UNSUPPORTED),
+    ({"dtype": 2}, fattn.FA_ERR_UNSUPPORTED),
+    ({"scale": float("nan")}, fattn.FA_ERR_INVALID_ARG),
+    ({"scale": float("inf")}, fattn.FA_ERR_INVALID_ARG),
+    ({"B": 1 << 16, "H": 1 << 16}, fattn.FA_ERR_INVALID_ARG),   # B*H too large
+    ({"B": 1 << 14, "H": 1 << 10, "N": 1 << 14, "D": 128}, fattn.FA_ERR_INVALID_ARG),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, status):
+    assert fwd(lib, **kw) == status
+
+
+def test_workspace_size(lib):
+    npad = 256
+    base = 2 * ((3 * 4 * npad * 4 + 255) // 256 * 256)
+    assert lib.fa_bwd_workspace_size(3, 4, 200, 64, 1) == base
+    assert lib.fa_bwd_workspace_size(3, 4, 200, 64, 0) == base + (3 * 4 * 200 * 64 * 4 + 255) // 256 * 256
+    assert lib.fa_bwd_workspace_size(3, 4, 200, 80, 0) == 0
+    assert lib.fa_bwd_workspace_size(0, 4, 200, 64, 0) == 0
+
+
+def bwd(lib, ws=FAKE, ws_bytes=1 << 40, D=64, deterministic=0, dq=FAKE, scale=0.125):
+    return lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, 1, 1, 128, D,
+                      ctypes.c_float(scale), 0, 0, deterministic, ws, ws_bytes, NULL)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    need = lib.fa_bwd_workspace_size(1, 1, 128, 64, 0)
+    assert bwd(lib, ws=NULL) == fattn.FA_ERR_INVALID_ARG
+    assert bwd(lib, ws=FAKE + 16) == fattn.FA_ERR_INVALID_ARG        # not 256-byte aligned
+    assert bwd(lib, ws_bytes=need - 1) == fattn.FA_ERR_INVALID_ARG   # too small
+    assert bwd(lib, dq=NULL) == fattn.FA_ERR_INVALID_ARG
+    assert bwd(lib, D=32) == fattn.FA_ERR_UNSUPPORTED
+    assert bwd(lib, scale=float("nan")) == fattn.FA_ERR_INVALID_ARG
+    # the deterministic layout needs no dQ accumulator, so it is smaller
+    det = lib.fa_bwd_workspace_size(1, 1, 128, 64, 1)
+    assert det < need
+
+
+def test_stage_entry_points_reject_bad_arguments(lib):
+    f = ctypes.c_float(0.125)
+    assert lib.fa_bwd_preprocess(NULL, FAKE, FAKE, 1, 1, 128, 64, 0, 0, FAKE, 1 << 40, NULL) == 1
+    assert lib.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, f, 0, 0, 0, FAKE, 10,
+                           NULL) == 1
+    assert lib.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, f, 0, 0, NULL, 1 << 40,
+                         NULL) == 1
+    assert lib.fa_bwd_dq_convert(FAKE, 1, 1, 128, 64, f, 5, FAKE, 1 << 40, NULL) == 2
+    code = ctypes.c_int(0)
+    assert lib.fa_device_error(NULL, None) == 1
+    assert lib.fa_selftest_wait_timeout(0, NULL) == 1
+    assert lib.fa_selftest_wait_timeout(5000000, NULL) == 1
+    del code
+
+
+def test_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fattn.fa_fwd(q, q, q, q, torch.zeros(1, 1, 128), 0.125, False)
