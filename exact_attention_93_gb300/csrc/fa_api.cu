@@ -113,6 +113,10 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
 }
 
 }  // namespace
+
+// The error word for the current device, for entry points in other files.
+uint32_t* device_error_word() { return error_word_ptr(); }
+
 }  // namespace fa
 
 using namespace fa;

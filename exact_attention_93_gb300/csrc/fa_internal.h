@@ -42,4 +42,8 @@ cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float sca
                               cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 
+// Device address of the error word bounded waits write (current device), or
+// nullptr if it cannot be resolved.
+uint32_t* device_error_word();
+
 }  // namespace fa

@@ -72,6 +72,7 @@ def load(path: str | None = None):
             "fa_bwd_dq_convert": (i, [vp, i, i, i, i, f, i, vp, sz, vp]),
             "fa_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
             "fa_selftest_wait_timeout": (i, [i, vp]),
+            "fa_bwd_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -200,6 +201,19 @@ def fa_bwd_dq_convert(dq, scale, workspace, stream=None):
     st = load().fa_bwd_dq_convert(_ptr(dq), B, H, N, D, float(scale), _dtype_code(dq),
                                   _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "fa_bwd_dq_convert")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, scale: float, causal: bool, stream=None):
+    """dQ, dK, dV with no workspace: for callers that cannot allocate device
+    memory.  Same result as the deterministic fa_bwd; its scratch is a fixed
+    array inside the library (see fa_bwd_noalloc in include/fattn.h for the
+    size limit and the rule that overlapping calls race)."""
+    _check_tensors(q, k, v, o, lse, do, dq, dk, dv)
+    B, H, N, D = _shape(q)
+    st = load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, D, float(scale),
+                               int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check(st, "fa_bwd_noalloc")
 
 
 def fa_device_error(stream=None) -> int:

@@ -145,6 +145,36 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int D, float scale, f
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass without any device allocation by the caller or the library.
+ * The pages describe nothing like it; it exists for callers that cannot hand
+ * over a workspace -- for example a plug-in run inside another framework's
+ * execution step that receives only its tensors and no allocator, or a
+ * latency-bound caller that cannot afford cudaMalloc (which may synchronise
+ * the whole device) in the middle of a step.
+ *
+ * Computes exactly what fa_bwd(..., deterministic = 1, ...) computes, with the
+ * same kernels; its scratch (the padded log2-LSE and Di rows, 8 bytes per
+ * query row rounded up to 128-row tiles, i.e. 8 * B*H*ceil(N/128)*128 bytes
+ * plus alignment) lives in one fixed array of FA_NOALLOC_SCRATCH_BYTES that
+ * the library places in device memory on every GPU where it is loaded, held
+ * until the process exits.
+ *   - Shapes whose scratch would not fit return FA_ERR_UNSUPPORTED before
+ *     anything is enqueued (B*H*ceil(N/128)*128 may be at most 2^20 rows).
+ *   - The first call on a device resolves the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, and each call overwrites
+ *     it completely.  Calls whose work can overlap on the GPU (different
+ *     streams, no ordering between them) race on it: order them on one stream.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int D, float scale, int causal, fa_dtype dtype,
+                         void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits write.  *code receives FA_OK or FA_ERR_TIMEOUT.  Returns
  * FA_ERR_CUDA if the synchronisation or the read fails.

@@ -10,7 +10,7 @@ from exact_attention_93_gb300 import build, fattn
 
 NULL = None
 EXPECTED = [
-    "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert",
+    "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert", "fa_bwd_noalloc",
     "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_device_error", "fa_fwd",
     "fa_selftest_wait_timeout", "fa_status_string",
 ]
