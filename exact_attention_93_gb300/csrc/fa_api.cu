@@ -72,13 +72,14 @@ fa_status check_ws(const Shape& s, int deterministic, const void* ws, size_t byt
   return FA_OK;
 }
 
-bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype) {
+bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype, int box_rows = kTile) {
   return make_tmap_3d(m, base,
                       dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                       2, static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.N),
                       static_cast<uint64_t>(s.BH()), static_cast<uint64_t>(s.D),
-                      static_cast<uint64_t>(s.N) * s.D, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+                      static_cast<uint64_t>(s.N) * s.D, 64, static_cast<uint32_t>(box_rows),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
@@ -91,7 +92,8 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
                           int causal, int dtype, int deterministic, void* ws) {
   *a = BwdLaunch{};
   if (!tile_map(&a->map_q, q, s, dtype) || !tile_map(&a->map_k, k, s, dtype) ||
-      !tile_map(&a->map_v, v, s, dtype) || !tile_map(&a->map_do, dO, s, dtype))
+      !tile_map(&a->map_v, v, s, dtype) || !tile_map(&a->map_do, dO, s, dtype) ||
+      !tile_map(&a->map_q64, q, s, dtype, 64) || !tile_map(&a->map_do64, dO, s, dtype, 64))
     return FA_ERR_CUDA;
   if (dq && !tile_map(&a->map_dq, dq, s, dtype)) return FA_ERR_CUDA;
   if (dk && !tile_map(&a->map_dk, dk, s, dtype)) return FA_ERR_CUDA;

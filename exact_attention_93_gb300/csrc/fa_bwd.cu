@@ -389,6 +389,315 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
+// dK / dV for D = 128, software-pipelined over 64-row query tiles
+// ---------------------------------------------------------------------------
+// With 64-row query tiles the scores and their gradient take 64 TMEM columns
+// each, so two iterations' S^T / dP^T fit beside the dV and dK accumulators:
+//   TMEM [128b, 128b + 64)       S^T of buffer b   (later dQ^T of that tile)
+//   TMEM [128b + 64, 128b + 128) dP^T of buffer b  (P^T packed over it)
+//   TMEM [256, 384) dV, [384, 512) dK
+// The MMA thread issues S^T / dP^T of tile i before dV / dK / dQ^T of tile
+// i - 1, so the tensor core always has the next products queued while the
+// eight elementwise warps work.  Q / dO (and their LSE / Di rows) come
+// through a three-stage ring.  dQ is formed transposed, dQ^T = K^T dS^T
+// (M = D), so TMEM lane = column d and every atomic warp instruction covers
+// 32 consecutive floats of one dQ row.
+constexpr int kD128Threads = 320;  // warps 0-7 elementwise, 8 producer, 9 MMA
+constexpr int kQ64 = 64;
+
+struct Dkdv128Smem {
+  static constexpr int kKBlock = kTile * 128;  // 128 rows x 128 B
+  static constexpr int kQBlock = kQ64 * 128;   // 64 rows x 128 B
+  alignas(1024) uint8_t k[2 * kKBlock];        // [D block][128 keys][64 d]
+  alignas(1024) uint8_t v[2 * kKBlock];
+  alignas(1024) uint8_t q[3][2 * kQBlock];     // [stage][D block][64 queries][64 d]
+  alignas(1024) uint8_t dO[3][2 * kQBlock];
+  alignas(1024) uint8_t dst[2][kKBlock];       // [buffer][128 keys][64 queries]
+  alignas(16) float lse2[3][kQ64];
+  alignas(16) float di[3][kQ64];
+  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], mma_done[2], tmem_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <bool kBf16, bool kCausal, bool kAtomicDq>
+__global__ void __launch_bounds__(kD128Threads, 1)
+    bwd_dkdv_d128_kernel(const __grid_constant__ BwdLaunch p) {
+  constexpr int D = 128;
+  using Smem = Dkdv128Smem;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_kt = (p.N + kTile - 1) / kTile;
+  const int Npad = n_kt * kTile;
+  const int n_q64 = (p.N + kQ64 - 1) / kQ64;
+  int kt, bh;
+  if (kCausal) {
+    kt = static_cast<int>(blockIdx.x / p.BH);
+    bh = static_cast<int>(blockIdx.x % p.BH);
+  } else {
+    kt = static_cast<int>(blockIdx.x % n_kt);
+    bh = static_cast<int>(blockIdx.x / n_kt);
+  }
+  const int k0 = kt * kTile;
+  const int it_begin = kCausal ? 2 * kt : 0;  // first 64-row query tile that sees a key here
+  const int n_it = n_q64 - it_begin;
+
+  if (tid == 0) {
+    mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s.qdo_full[i], 1);
+      mbar_init(&s.qdo_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 256);
+      mbar_init(&s.mma_done[i], 1);
+      mbar_init(&s.tmem_free[i], 256);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  const uint32_t tdV = tbase + 256, tdK = tbase + 384;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.kv_full, 4 * Smem::kKBlock);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(s.k + kb * Smem::kKBlock, &p.map_k, &s.kv_full, kb * 64, k0, bh);
+        tma_load_3d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % 3;
+        if (it >= 3 && !mbar_wait(&s.qdo_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
+        const int q0 = (it_begin + it) * kQ64;
+        mbar_arrive_expect_tx(&s.qdo_full[st], 4 * Smem::kQBlock + 2 * kQ64 * 4);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, bh);
+          tma_load_3d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0,
+                      bh);
+        }
+        const long long off = static_cast<long long>(bh) * Npad + q0;
+        bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
+        bulk_load(s.di[st], p.di + off, kQ64 * 4, &s.qdo_full[st]);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        int zero = 0;
+        mbar_wait(&s.kv_full, 0, p.err, &zero, 100000000ull);
+        for (int t = max(0, issued - 3); t < issued; ++t)
+          mbar_wait(&s.qdo_full[t % 3], (t / 3) & 1, p.err, &zero, 100000000ull);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ab = kBf16 ? 1u : 0u;
+      constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
+      constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
+      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);  // d x queries, over keys
+      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
+      for (int it = 0; ok && it <= n_it; ++it) {
+        if (it < n_it) {
+          const int b = it & 1, st = it % 3;
+          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
+          if (kAtomicDq && it >= 2 &&
+              !mbar_wait(&s.tmem_free[b], ((it - 2) >> 1) & 1, p.err, abort_flag))
+            break;
+          tc_fence_after();
+          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+            tc_mma_ss(tbase + b * 128, smem_desc_sw128(k_addr + ka, 16, 1024),
+                      smem_desc_sw128(q_addr + kq, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+            tc_mma_ss(tbase + b * 128 + 64, smem_desc_sw128(v_addr + ka, 16, 1024),
+                      smem_desc_sw128(do_addr + kq, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s.s_full[b]);
+        }
+        if (it >= 1) {
+          const int j = it - 1, b = j & 1, st = j % 3;
+          if (!mbar_wait(&s.p_full[b], (j >> 1) & 1, p.err, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+          const uint32_t dst_addr = smem_u32(s.dst[b]);
+          // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
+#pragma unroll
+          for (int kk = 0; kk < kQ64 / 16; ++kk)
+            tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                      smem_desc_sw128(do_addr + kk * 16 * 128, Smem::kQBlock, 1024), idKV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q : A = dS^T in smem (K-major over queries)
+#pragma unroll
+          for (int kk = 0; kk < kQ64 / 16; ++kk)
+            tc_mma_ss(tdK, smem_desc_sw128(dst_addr + kk * 32, 16, 1024),
+                      smem_desc_sw128(q_addr + kk * 16 * 128, Smem::kQBlock, 1024), idKV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          if (kAtomicDq) {
+            // dQ^T = K^T dS^T : A = K read MN-major, B = dS^T read MN-major
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc_mma_ss(tbase + b * 128,
+                        smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kKBlock, 1024),
+                        smem_desc_sw128(dst_addr + kk * 16 * 128, Smem::kKBlock, 1024), idQ,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s.mma_done[b]);
+          tc_commit(&s.qdo_empty[st]);
+        }
+      }
+      tc_commit(&s.drain);
+      int zero = 0;
+      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, query-column half
+    const int r = quad * 32 + lane;                // key row (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+
+    // dQ^T of tile j: lane = column d, this warp's 32 query columns
+    auto flush_dq = [&](int j) -> bool {
+      const int bj = j & 1;
+      if (!warp_wait(&s.mma_done[bj], (j >> 1) & 1, p.err, abort_flag)) return false;
+      tc_fence_after();
+      uint32_t g[32];
+      tmem_ld32(tbase + lane_off + bj * 128 + half * 32, g);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.tmem_free[bj]);
+      const int qbase = (it_begin + j) * kQ64 + half * 32;
+      float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + qbase) * D + r;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (qbase + c < p.N) atomicAdd(dst + static_cast<long long>(c) * D, __uint_as_float(g[c]));
+      return true;
+    };
+
+    for (int it = 0; it < n_it; ++it) {
+      const int b = it & 1, st = it % 3;
+      const int q0 = (it_begin + it) * kQ64;
+      bool w = warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) &&
+               warp_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag);
+      // dS^T buffer b was last read by the products of tile it - 2
+      if (w && !kAtomicDq && it >= 2)
+        w = warp_wait(&s.mma_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag);
+      if (!w) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
+      tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
+      tmem_ld_wait();
+      const bool diag = kCausal && (q0 < k0 + kTile);
+      const int key = k0 + r;
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
+        const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
+        const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
+          if (diag && key > q0 + half * 32 + t + e) pe = 0.f;
+          pv[e] = pe;
+          dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
+        }
+        pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
+        pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
+        dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
+        dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
+      }
+      // P^T over this warp's own dP^T columns (already read)
+      tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
+      store_row_chunk_sw128(s.dst[b], r, half, dk);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[b]);
+      if (kAtomicDq && it >= 1 && !flush_dq(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && kAtomicDq) ok = flush_dq(n_it - 1);
+
+    // ---------------------------------------------------------- epilogue
+    bool done = ok;
+    if (ok && !kAtomicDq)
+      done = warp_wait(&s.mma_done[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, p.err, abort_flag);
+    if (named_bar_and(1, 256, done)) {
+      tc_fence_after();
+      uint8_t* dk_tile = s.q[0];   // 32 KB of the free query ring
+      uint8_t* dv_tile = s.dO[0];
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // this warp's 64 d columns, 32 at a time
+        const int c32 = half * 2 + c;
+        uint32_t a[32], g[32];
+        tmem_ld32(tdV + lane_off + c32 * 32, a);
+        tmem_ld32(tdK + lane_off + c32 * 32, g);
+        tmem_ld_wait();
+        uint32_t pa[16], pb[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          pa[t] = pack2<kBf16>(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
+          pb[t] = pack2<kBf16>(__uint_as_float(g[2 * t]) * p.scale,
+                               __uint_as_float(g[2 * t + 1]) * p.scale);
+        }
+        store_row_chunk_sw128(dv_tile, r, c32, pa);
+        store_row_chunk_sw128(dk_tile, r, c32, pb);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (tid == 0) {
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_store_3d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, bh);
+          tma_store_3d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // deterministic dQ
 // ---------------------------------------------------------------------------
 template <int D>
@@ -670,9 +979,27 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <bool kBf16, bool kCausal, bool kAtomic>
+cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
+  auto kern = bwd_dkdv_d128_kernel<kBf16, kCausal, kAtomic>;
+  const int smem = static_cast<int>(sizeof(Dkdv128Smem)) + 1024;
+  static bool configured = false;
+  cudaError_t e = set_smem(kern, smem, configured);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), kD128Threads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D, bool kBf16>
 cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
   const bool atomic = a.dq_accum != nullptr;
+  if (D == 128) {
+    if (a.causal)
+      return atomic ? launch_dkdv128_t<kBf16, true, true>(a, st) : launch_dkdv128_t<kBf16, true, false>(a, st);
+    return atomic ? launch_dkdv128_t<kBf16, false, true>(a, st) : launch_dkdv128_t<kBf16, false, false>(a, st);
+  }
   if (a.causal)
     return atomic ? launch_dkdv_t<D, kBf16, true, true>(a, st) : launch_dkdv_t<D, kBf16, true, false>(a, st);
   return atomic ? launch_dkdv_t<D, kBf16, false, true>(a, st) : launch_dkdv_t<D, kBf16, false, false>(a, st);

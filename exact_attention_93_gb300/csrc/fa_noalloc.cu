@@ -49,13 +49,15 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool tile_map(CUtensorMap* m, const void* base, int N, long long BH, int D, int dtype) {
+bool tile_map(CUtensorMap* m, const void* base, int N, long long BH, int D, int dtype,
+              int box_rows = kTile) {
   return make_tmap_3d(m, base,
                       dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                       2, static_cast<uint64_t>(D), static_cast<uint64_t>(N),
                       static_cast<uint64_t>(BH), static_cast<uint64_t>(D),
-                      static_cast<uint64_t>(N) * D, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+                      static_cast<uint64_t>(N) * D, 64, static_cast<uint32_t>(box_rows),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -90,7 +92,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (!tile_map(&a.map_q, q, N, BH, D, dtype) || !tile_map(&a.map_k, k, N, BH, D, dtype) ||
       !tile_map(&a.map_v, v, N, BH, D, dtype) || !tile_map(&a.map_do, dO, N, BH, D, dtype) ||
       !tile_map(&a.map_dq, dq, N, BH, D, dtype) || !tile_map(&a.map_dk, dk, N, BH, D, dtype) ||
-      !tile_map(&a.map_dv, dv, N, BH, D, dtype))
+      !tile_map(&a.map_dv, dv, N, BH, D, dtype) || !tile_map(&a.map_q64, q, N, BH, D, dtype, 64) ||
+      !tile_map(&a.map_do64, dO, N, BH, D, dtype, 64))
     return FA_ERR_CUDA;
   float* lse2 = reinterpret_cast<float*>(scratch);
   float* di = reinterpret_cast<float*>(scratch + di_off);
