@@ -142,14 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int Npad = n_tiles * kTile;
-  int kt, bh;
-  if (kCausal) {  // key tiles near the start see the most queries: first
-    kt = static_cast<int>(blockIdx.x / p.BH);
-    bh = static_cast<int>(blockIdx.x % p.BH);
-  } else {
-    kt = static_cast<int>(blockIdx.x % n_tiles);
-    bh = static_cast<int>(blockIdx.x / n_tiles);
-  }
+  // Head-major; key tiles near the start see the most queries and go first.
+  const int bh = static_cast<int>(blockIdx.x / n_tiles);
+  const int kt = static_cast<int>(blockIdx.x % n_tiles);
   const int k0 = kt * kTile;
   const int it_begin = kCausal ? kt : 0;
   const int n_it = n_tiles - it_begin;
@@ -225,14 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tS, smem_desc_sw128(k_addr + off, 16, 1024),
-                    smem_desc_sw128(q_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tS, desc_add(smem_desc_sw128(k_addr, 16, 1024), off),
+                    desc_add(smem_desc_sw128(q_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdP, smem_desc_sw128(v_addr + off, 16, 1024),
-                    smem_desc_sw128(do_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tdP, desc_add(smem_desc_sw128(v_addr, 16, 1024), off),
+                    desc_add(smem_desc_sw128(do_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s.s_full);
         if (!mbar_wait(&s.p_full, it & 1, p.err, abort_flag)) break;
@@ -240,22 +235,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // dV += P^T dO : A = P^T in TMEM (16-bit pairs over S^T columns [0, 64))
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tdV, tS + kk * 8, smem_desc_sw128(do_addr + kk * 16 * 128, Smem::kBlockBytes, 1024),
+          tc_mma_ts(tdV, tS + kk * 8, desc_add(smem_desc_sw128(do_addr, Smem::kBlockBytes, 1024), kk * 16 * 128),
                     idKM, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q : A = dS^T in smem, K-major over queries
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdK, smem_desc_sw128(dst_addr + aoff, 16, 1024),
-                    smem_desc_sw128(q_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idKM,
+          tc_mma_ss(tdK, desc_add(smem_desc_sw128(dst_addr, 16, 1024), aoff),
+                    desc_add(smem_desc_sw128(q_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idKM,
                     (it > 0 || kk > 0) ? 1u : 0u);
         }
         if (kAtomicDq) {
           // dQ_i = dS K : A = dS (queries x keys) read MN-major from dS^T
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_ss(tdQ, smem_desc_sw128(dst_addr + kk * 16 * 128, Smem::kBlockBytes, 1024),
-                      smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idMM,
+            tc_mma_ss(tdQ, desc_add(smem_desc_sw128(dst_addr, Smem::kBlockBytes, 1024), kk * 16 * 128),
+                      desc_add(smem_desc_sw128(k_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idMM,
                       kk > 0 ? 1u : 0u);
         }
         tc_commit(&s.mma_done);
@@ -392,17 +387,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 // dK / dV for D = 128, software-pipelined over 64-row query tiles
 // ---------------------------------------------------------------------------
 // With 64-row query tiles the scores and their gradient take 64 TMEM columns
-// each, so two iterations' S^T / dP^T fit beside the dV and dK accumulators:
-//   TMEM [128b, 128b + 64)       S^T of buffer b   (later dQ^T of that tile)
-//   TMEM [128b + 64, 128b + 128) dP^T of buffer b  (P^T packed over it)
+// each, so two tiles' S^T / dP^T fit beside the dV and dK accumulators:
+//   TMEM [128b, 128b + 64)       buffer b: S^T of tile i (b = i & 1), then
+//                                dQ^T of tile i - 1 once S^T is consumed
+//   TMEM [128b + 64, 128b + 128) buffer b: dP^T of tile i; then, for each
+//                                32-query half, P^T and dS^T packed over it
 //   TMEM [256, 384) dV, [384, 512) dK
-// The MMA thread issues S^T / dP^T of tile i before dV / dK / dQ^T of tile
-// i - 1, so the tensor core always has the next products queued while the
-// eight elementwise warps work.  Q / dO (and their LSE / Di rows) come
-// through a three-stage ring.  dQ is formed transposed, dQ^T = K^T dS^T
-// (M = D), so TMEM lane = column d and every atomic warp instruction covers
-// 32 consecutive floats of one dQ row.
-constexpr int kD128Threads = 320;  // warps 0-7 elementwise, 8 producer, 9 MMA
+// The tensor core's order is
+//   S^T,dP^T(i) | dQ^T(i-2) | dV,dK(i-1) | S^T,dP^T(i+1) | dQ^T(i-1) | ...
+// so the scores of the next tile are always queued while the elementwise
+// warps work on the current one.  dQ^T(i-2) takes the S^T columns of tile
+// i-1 once those are consumed, and the dV/dK products that follow give the
+// four dQ warps time to drain it before S^T(i+1) reuses the buffer.  Q / dO (with
+// their LSE / Di rows) come through a three-stage ring; eight warps do the
+// elementwise work.  dV and dK take their A operands (P^T, dS^T) from TMEM,
+// so they read only dO or Q from shared memory; the tensor core's operand
+// bandwidth from shared memory (about 64 bytes per clock) is what bounds the
+// S^T / dP^T and dQ^T products, whose A comes from shared memory.
+// dQ is formed transposed, dQ^T = K^T dS^T (M = D), so
+// TMEM lane = column d and each atomic warp instruction covers 32
+// consecutive floats of one dQ row.  Because the tensor core completes
+// products in issue order, "S^T(i) is ready" also means dK(i-2) is done;
+// dQ^T(i-2), the other reader of dS^T buffer i & 1, is waited for apart.
+constexpr int kD128Threads = 448;  // warps 0-7 elementwise, 8-11 dQ, 12 producer, 13 MMA
 constexpr int kQ64 = 64;
 
 struct Dkdv128Smem {
@@ -415,8 +422,8 @@ struct Dkdv128Smem {
   alignas(1024) uint8_t dst[2][kKBlock];       // [buffer][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
-  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], mma_done[2], tmem_free[2];
-  uint64_t drain;
+  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], dq_full[2], tmem_free[2];
+  uint64_t all_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -433,14 +440,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   const int n_kt = (p.N + kTile - 1) / kTile;
   const int Npad = n_kt * kTile;
   const int n_q64 = (p.N + kQ64 - 1) / kQ64;
-  int kt, bh;
-  if (kCausal) {
-    kt = static_cast<int>(blockIdx.x / p.BH);
-    bh = static_cast<int>(blockIdx.x % p.BH);
-  } else {
-    kt = static_cast<int>(blockIdx.x % n_kt);
-    bh = static_cast<int>(blockIdx.x / n_kt);
-  }
+  // Head-major order, longest key tiles first within a head: the CTAs in
+  // flight share one head's Q, dO and dQ accumulator in L2.
+  const int bh = static_cast<int>(blockIdx.x / n_kt);
+  const int kt = static_cast<int>(blockIdx.x % n_kt);
   const int k0 = kt * kTile;
   const int it_begin = kCausal ? 2 * kt : 0;  // first 64-row query tile that sees a key here
   const int n_it = n_q64 - it_begin;
@@ -454,14 +457,15 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
-      mbar_init(&s.mma_done[i], 1);
-      mbar_init(&s.tmem_free[i], 256);
+      mbar_init(&s.dq_full[i], 1);
+      mbar_init(&s.tmem_free[i], 128);
     }
+    mbar_init(&s.all_done, 1);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   const uint32_t tdV = tbase + 256, tdK = tbase + 384;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       mbar_arrive_expect_tx(&s.kv_full, 4 * Smem::kKBlock);
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           mbar_wait(&s.qdo_full[t % 3], (t / 3) & 1, p.err, &zero, 100000000ull);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t ab = kBf16 ? 1u : 0u;
@@ -512,65 +516,106 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);  // d x queries, over keys
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
+      // dQ^T(j) = K^T dS^T(j), issued once S^T(j + 1) is consumed, into the
+      // S^T columns of buffer (j + 1) & 1.
+      auto issue_dq = [&](int j) {
+        const uint32_t dst_addr = smem_u32(s.dst[j & 1]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_ss(tbase + ((j + 1) & 1) * 128,
+                    desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
+                    desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
+                    kk > 0 ? 1u : 0u);
+        tc_commit(&s.dq_full[j & 1]);
+      };
       for (int it = 0; ok && it <= n_it; ++it) {
         if (it < n_it) {
           const int b = it & 1, st = it % 3;
-          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
-          if (kAtomicDq && it >= 2 &&
-              !mbar_wait(&s.tmem_free[b], ((it - 2) >> 1) & 1, p.err, abort_flag))
+          // Buffer b last held dQ^T(it - 3); it must be drained before reuse.
+          if (kAtomicDq && it >= 3 &&
+              !mbar_wait(&s.tmem_free[b], ((it - 3) >> 1) & 1, p.err, abort_flag))
             break;
+          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
           tc_fence_after();
           const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
             const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            tc_mma_ss(tbase + b * 128, smem_desc_sw128(k_addr + ka, 16, 1024),
-                      smem_desc_sw128(q_addr + kq, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
+                      desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
             const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            tc_mma_ss(tbase + b * 128 + 64, smem_desc_sw128(v_addr + ka, 16, 1024),
-                      smem_desc_sw128(do_addr + kq, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
+                      desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
           }
           tc_commit(&s.s_full[b]);
         }
         if (it >= 1) {
-          const int j = it - 1, b = j & 1, st = j % 3;
-          if (!mbar_wait(&s.p_full[b], (j >> 1) & 1, p.err, abort_flag)) break;
+          const int j = it - 1, bj = j & 1, st = j % 3;
+          if (!mbar_wait(&s.p_full[bj], (j >> 1) & 1, p.err, abort_flag)) break;
           tc_fence_after();
+          // S^T(j) is consumed: dQ^T(j - 1) can take its columns.
+          if (kAtomicDq && j >= 1) issue_dq(j - 1);
           const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-          const uint32_t dst_addr = smem_u32(s.dst[b]);
           // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
 #pragma unroll
           for (int kk = 0; kk < kQ64 / 16; ++kk)
-            tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                      smem_desc_sw128(do_addr + kk * 16 * 128, Smem::kQBlock, 1024), idKV,
+            tc_mma_ts(tdV, tbase + bj * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                      desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                       (j > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q : A = dS^T in smem (K-major over queries)
+          // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
 #pragma unroll
           for (int kk = 0; kk < kQ64 / 16; ++kk)
-            tc_mma_ss(tdK, smem_desc_sw128(dst_addr + kk * 32, 16, 1024),
-                      smem_desc_sw128(q_addr + kk * 16 * 128, Smem::kQBlock, 1024), idKV,
+            tc_mma_ts(tdK, tbase + bj * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                      desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                       (j > 0 || kk > 0) ? 1u : 0u);
-          if (kAtomicDq) {
-            // dQ^T = K^T dS^T : A = K read MN-major, B = dS^T read MN-major
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              tc_mma_ss(tbase + b * 128,
-                        smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kKBlock, 1024),
-                        smem_desc_sw128(dst_addr + kk * 16 * 128, Smem::kKBlock, 1024), idQ,
-                        kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&s.mma_done[b]);
           tc_commit(&s.qdo_empty[st]);
         }
       }
+      // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
+      // has left it.
+      if (ok && kAtomicDq && !*abort_flag) {
+        const int j = n_it - 1;
+        if (j < 2 || mbar_wait(&s.tmem_free[(j + 1) & 1], ((j - 2) >> 1) & 1, p.err, abort_flag)) {
+          tc_fence_after();
+          issue_dq(j);
+        }
+      }
+      tc_commit(&s.all_done);
       tc_commit(&s.drain);
       int zero = 0;
       mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain
+    if (kAtomicDq) {
+      const int quad = warp & 3;
+      const int d = quad * 32 + lane;  // TMEM lane = column d of dQ
+      const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+      for (int j = 0; j < n_it; ++j) {
+        if (!warp_wait(&s.dq_full[j & 1], (j >> 1) & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const int b = (j + 1) & 1;  // dQ^T(j) sits in the S^T columns of tile j + 1
+        uint32_t g[2][32];
+        tmem_ld32(tbase + lane_off + b * 128, g[0]);
+        tmem_ld32(tbase + lane_off + b * 128 + 32, g[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s.tmem_free[b]);
+        const int q0 = (it_begin + j) * kQ64;
+        float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
+        const int nq = min(kQ64, p.N - q0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (h * 32 + c < nq)
+              atomicAdd(dst + static_cast<long long>(h * 32 + c) * D, __uint_as_float(g[h][c]));
+      }
     }
   } else {
     // ------------------------------------------------------------ elementwise
@@ -579,34 +624,13 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
-
-    // dQ^T of tile j: lane = column d, this warp's 32 query columns
-    auto flush_dq = [&](int j) -> bool {
-      const int bj = j & 1;
-      if (!warp_wait(&s.mma_done[bj], (j >> 1) & 1, p.err, abort_flag)) return false;
-      tc_fence_after();
-      uint32_t g[32];
-      tmem_ld32(tbase + lane_off + bj * 128 + half * 32, g);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&s.tmem_free[bj]);
-      const int qbase = (it_begin + j) * kQ64 + half * 32;
-      float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + qbase) * D + r;
-#pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (qbase + c < p.N) atomicAdd(dst + static_cast<long long>(c) * D, __uint_as_float(g[c]));
-      return true;
-    };
-
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1, st = it % 3;
       const int q0 = (it_begin + it) * kQ64;
-      bool w = warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) &&
-               warp_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag);
-      // dS^T buffer b was last read by the products of tile it - 2
-      if (w && !kAtomicDq && it >= 2)
-        w = warp_wait(&s.mma_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag);
-      if (!w) {
+      // s_full also implies that the products of tile it - 2 (the last
+      // readers of dS^T buffer b) are complete.
+      if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) ||
+          !warp_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
@@ -637,24 +661,26 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
         dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
       }
-      // P^T over this warp's own dP^T columns (already read)
+      // P^T and dS^T over this warp's own 32 dP^T columns (already read):
+      // P^T in the first 16, dS^T in the next 16.
       tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
-      store_row_chunk_sw128(s.dst[b], r, half, dk);
+      tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32 + 16, dk);
+      if (kAtomicDq) {
+        // dQ^T(it - 2) reads dS^T buffer b and is issued after S^T(it)
+        if (it >= 2 && !warp_wait(&s.dq_full[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        store_row_chunk_sw128(s.dst[b], r, half, dk);
+      }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.p_full[b]);
-      if (kAtomicDq && it >= 1 && !flush_dq(it - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && kAtomicDq) ok = flush_dq(n_it - 1);
 
     // ---------------------------------------------------------- epilogue
-    bool done = ok;
-    if (ok && !kAtomicDq)
-      done = warp_wait(&s.mma_done[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, p.err, abort_flag);
+    const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
     if (named_bar_and(1, 256, done)) {
       tc_fence_after();
       uint8_t* dk_tile = s.q[0];   // 32 KB of the free query ring
@@ -691,7 +717,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -724,14 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int Npad = n_tiles * kTile;
-  int qt, bh;
-  if (kCausal) {
-    qt = n_tiles - 1 - static_cast<int>(blockIdx.x / p.BH);
-    bh = static_cast<int>(blockIdx.x % p.BH);
-  } else {
-    qt = static_cast<int>(blockIdx.x % n_tiles);
-    bh = static_cast<int>(blockIdx.x / n_tiles);
-  }
+  // Head-major; under the causal mask the longest query tiles go first.
+  const int bh = static_cast<int>(blockIdx.x / n_tiles);
+  const int qt = kCausal ? n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles)
+                         : static_cast<int>(blockIdx.x % n_tiles);
   const int q0 = qt * kTile;
   const int n_kv = kCausal ? qt + 1 : n_tiles;
 
@@ -801,14 +823,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tS, smem_desc_sw128(q_addr + off, 16, 1024),
-                    smem_desc_sw128(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tS, desc_add(smem_desc_sw128(q_addr, 16, 1024), off),
+                    desc_add(smem_desc_sw128(k_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdP, smem_desc_sw128(do_addr + off, 16, 1024),
-                    smem_desc_sw128(v_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tdP, desc_add(smem_desc_sw128(do_addr, 16, 1024), off),
+                    desc_add(smem_desc_sw128(v_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s.s_full);
         tc_commit(&s.v_empty);
@@ -818,8 +840,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdQ, smem_desc_sw128(ds_addr + aoff, 16, 1024),
-                    smem_desc_sw128(k_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idKM,
+          tc_mma_ss(tdQ, desc_add(smem_desc_sw128(ds_addr, 16, 1024), aoff),
+                    desc_add(smem_desc_sw128(k_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idKM,
                     (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&s.mma_done);

@@ -19,7 +19,11 @@
 //              S_{j+1} is issued before PV_j so the tensor core computes the
 //              next scores while the softmax warps work on the current ones.
 //
-// TMEM columns: [0,128) S/P buffer 0, [128,256) S/P buffer 1, [256,256+D) O.
+// TMEM columns: [0,128) S/P buffer 0, [128,256) S/P buffer 1, [256,256+D) O,
+// [256+D, 256+3D/2) Q.  The tensor core reads its operands from shared memory
+// at roughly 64 bytes per clock, so every product keeps its A operand in TMEM
+// (Q for S = Q K^T, P for O += P V) and reads only B (K or V) from shared
+// memory: one 4 KB B slice per 64-cycle instruction keeps it fed.
 //
 // Softmax bookkeeping works in log2 units: scores are multiplied by
 // scale*log2(e) and exponentiated with ex2.  The reference maximum m is only
@@ -29,7 +33,7 @@
 //
 // Causal mask (walkthrough sec. 5.3): query i sees keys j <= i.  Key tiles
 // past the diagonal are never loaded; the diagonal tile and a ragged last
-// tile are masked element-wise.  Query tiles are scheduled longest first.
+// tile are masked element-wise.  Within a head, the longest query tiles go first.
 #include <climits>
 
 #include "fa_internal.h"
@@ -53,7 +57,7 @@ struct FwdSmem {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done, drain;
+  uint64_t o_done, drain, qt_full;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -73,14 +77,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int n_q_tiles = (p.N + kTile - 1) / kTile;
-  int qt, bh;
-  if (kCausal) {  // longest rows first
-    qt = n_q_tiles - 1 - static_cast<int>(blockIdx.x / p.BH);
-    bh = static_cast<int>(blockIdx.x % p.BH);
-  } else {        // neighbouring CTAs share one head's K and V in L2
-    qt = static_cast<int>(blockIdx.x % n_q_tiles);
-    bh = static_cast<int>(blockIdx.x / n_q_tiles);
-  }
+  // Head-major order, so that the CTAs in flight share one head's K and V in
+  // L2; under the causal mask the longest query tiles of a head go first.
+  const int bh = static_cast<int>(blockIdx.x / n_q_tiles);
+  const int qt = kCausal ? n_q_tiles - 1 - static_cast<int>(blockIdx.x % n_q_tiles)
+                         : static_cast<int>(blockIdx.x % n_q_tiles);
   const int q0 = qt * kTile;
   const int n_kv = (p.N + kTile - 1) / kTile;
   const int n_tiles = kCausal ? min(n_kv, qt + 1) : n_kv;
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     }
     mbar_init(&s.o_done, 1);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.qt_full, 128);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
   const uint32_t tO = tbase + 256;
+  const uint32_t tQ = tbase + 256 + D;  // Q as the A operand of S = Q K^T (D/2 columns)
   volatile int* abort_flag = &s.abort_flag;
 
   if (warp == 4) {
@@ -156,20 +159,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       constexpr uint32_t ab = kBf16 ? 1u : 0u;
       constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
       constexpr uint32_t idPV = idesc_f16(128, D, ab, 0, 1);
-      const uint32_t q_addr = smem_u32(s.q);
-      bool ok = mbar_wait(&s.q_full, 0, p.err, abort_flag);
+      // Operand descriptors are built once and advanced by constant offsets.
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(s.v[0]), Smem::kBlockBytes, 1024);
+      bool ok = mbar_wait(&s.qt_full, 0, p.err, abort_flag);
       for (int j = 0; ok && j <= n_tiles; ++j) {
         if (j < n_tiles) {
           const int st = j & 1;
           const uint32_t u = static_cast<uint32_t>(j >> 1);
           if (!mbar_wait(&s.k_full[st], u & 1, p.err, abort_flag)) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(s.k[st]);
+          const uint64_t dk = desc_add(dk0, st * Smem::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-            tc_mma_ss(tbase + st * 128, smem_desc_sw128(q_addr + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            tc_mma_ts(tbase + st * 128, tQ + kk * 8, desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
           }
           tc_commit(&s.s_full[st]);
           tc_commit(&s.k_empty[st]);
@@ -180,11 +184,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           if (!mbar_wait(&s.p_full[st], u & 1, p.err, abort_flag)) break;
           if (!mbar_wait(&s.v_full[st], u & 1, p.err, abort_flag)) break;
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(s.v[st]);
+          const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_ts(tO, tbase + st * 128 + kk * 8,
-                      smem_desc_sw128(v_addr + kk * 16 * 128, Smem::kBlockBytes, 1024), idPV,
+            tc_mma_ts(tO, tbase + st * 128 + kk * 8, desc_add(dv, kk * 16 * 128), idPV,
                       (jj > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&s.o_done);
           tc_commit(&s.v_empty[st]);
@@ -204,8 +207,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const bool pos_scale = sl2 > 0.f;
     float m = -INFINITY;  // reference maximum, log2 units
     float l = 0.f;        // running sum of 2^(t - m)
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    // Q into TMEM, so that S = Q K^T reads only K from shared memory: thread
+    // r moves row r out of the swizzled tile (16-byte chunk c of a 128-byte
+    // row sits at chunk c ^ (r & 7)); the 16-bit pairs keep their order.
+    bool ok = warp_wait(&s.q_full, 0, p.err, abort_flag);
+    if (ok) {
+#pragma unroll
+      for (int kb = 0; kb < Smem::kBlocks; ++kb) {
+        uint32_t w[32];
+        const uint8_t* row = s.q + kb * Smem::kBlockBytes + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) * 16));
+          w[c * 4] = v.x;
+          w[c * 4 + 1] = v.y;
+          w[c * 4 + 2] = v.z;
+          w[c * 4 + 3] = v.w;
+        }
+        tmem_st32(tQ + lane_off + kb * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.qt_full);
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int st = j & 1;
       const uint32_t u = static_cast<uint32_t>(j >> 1);
       if (!warp_wait(&s.s_full[st], u & 1, p.err, abort_flag)) {
@@ -215,14 +240,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       tc_fence_after();
       float sv[kTile];
       {
-        uint32_t raw[32];
+        // All four loads in flight before the single wait.
+        uint32_t raw[kTile / 32][32];
 #pragma unroll
-        for (int c = 0; c < kTile / 32; ++c) {
-          tmem_ld32(tbase + lane_off + st * 128 + c * 32, raw);
-          tmem_ld_wait();
+        for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tbase + lane_off + st * 128 + c * 32, raw[c]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) sv[c * 32 + t] = __uint_as_float(raw[t]);
-        }
+        for (int c = 0; c < kTile / 32; ++c)
+#pragma unroll
+          for (int t = 0; t < 32; ++t) sv[c * 32 + t] = __uint_as_float(raw[c][t]);
       }
       // Scores -> log2 units.  With a positive scale this is folded into the
       // exponent below (one FFMA per score); otherwise scale first.
@@ -238,9 +264,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         for (int c = 0; c < kTile; ++c)
           if (c > last) sv[c] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // Row maximum with eight independent chains (short dependency depth).
+      float mxs[8];
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, sv[c]);
+      for (int t = 0; t < 8; ++t) mxs[t] = sv[t];
+#pragma unroll
+      for (int c = 8; c < kTile; c += 8)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mxs[t] = fmaxf(mxs[t], sv[c + t]);
+      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
       const float m_tile = pos_scale ? mx * sl2 : mx;
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + kRescaleThreshold;
@@ -268,7 +301,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
       }
       const float mneg = (m == -INFINITY) ? 0.f : -m;
-      float rowsum = 0.f;
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -277,12 +310,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           const float x0 = sv[h * 64 + 2 * c], x1 = sv[h * 64 + 2 * c + 1];
           const float p0 = ex2_approx(pos_scale ? fmaf(x0, sl2, mneg) : x0 + mneg);
           const float p1 = ex2_approx(pos_scale ? fmaf(x1, sl2, mneg) : x1 + mneg);
-          rowsum += p0 + p1;
+          sums[(c & 1) * 2] += p0;
+          sums[(c & 1) * 2 + 1] += p1;
           pk[c] = pack2<kBf16>(p0, p1);
         }
         tmem_st32(tbase + lane_off + st * 128 + h * 32, pk);
       }
-      l += rowsum;
+      l += (sums[0] + sums[1]) + (sums[2] + sums[3]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.p_full[st]);

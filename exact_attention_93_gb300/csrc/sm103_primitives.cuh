@@ -48,14 +48,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test-and-suspend: a thread whose phase is not complete sleeps in hardware
+// until the phase completes or `hint_ns` passes, instead of spinning on
+// shared memory (polling competes with the tensor core's operand reads).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -79,12 +83,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) break;
-    }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) break;
   }
   atomicExch(err, kDevErrTimeout);
   *abort_flag = 1;
@@ -288,6 +290,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= 1ull << 46;  // descriptor version for tcgen05
   d |= 2ull << 61;  // 128-byte swizzle
   return d;
+}
+
+// The same descriptor with its start moved by `bytes` (a multiple of 16).
+// The start field holds address >> 4 in 14 bits; shared-memory addresses stay
+// below 256 KB, so the addition never carries into the next field and a
+// base descriptor built once can be advanced with one add per operand.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
 // Instruction descriptor, .kind::f16 with fp32 accumulation.
