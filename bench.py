@@ -153,6 +153,22 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def slowest_rank(value: float, dist, device) -> float:
+    """The largest value over all ranks (the slowest rank's time); the value
+    itself on a single process."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """All ranks' work (each rank runs its own replica) over one step's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------
 # the CPU baseline: the fp64 oracle on a bounded sample of the workload
 # --------------------------------------------------------------------------
@@ -160,12 +176,12 @@ class ClockSampler:
 def oracle_sample(w, inputs, rows_per_head):
     """Rows of the workload whose whole forward + backward share the oracle
     computes: O, LSE, dQ for the row and its contributions to dK and dV."""
-    from exact_attention_93_gb300 import workloads as W
+    import numpy as np
     rows = []
     flops = 0.0
     for h in range(w.H):
-        r = W.sampled_rows(w, 0, h)
-        r = r[:: max(1, len(r) // rows_per_head)][:rows_per_head]
+        # evenly spaced query rows, so causal rows of every length are timed
+        r = np.unique(np.linspace(0, w.N - 1, min(rows_per_head, w.N)).astype(np.int64))
         rows.append(r)
         vis = (r + 1) if w.causal else [w.N] * len(r)
         flops += sum(14.0 * float(v) * w.D for v in vis)  # 4 fwd + 10 bwd per key per dim
@@ -195,7 +211,7 @@ def run_reference(args, w):
         return
     from exact_attention_93_gb300 import workloads as W
     inputs = W.make_inputs(w)
-    rows_per_head = 8
+    rows_per_head = 64
     for _ in range(args.warmup):
         time_oracle(w, inputs, 2)
     vals, secs = [], 0.0
@@ -291,15 +307,12 @@ def run_ours(args, w):
                   for i, n in enumerate(names)}
     if fattn.fa_device_error() != fattn.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait")
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank(total_ms, dist, dev)
 
     ms_step = total_ms / args.steps
     fwd_f, bwd_f = w.fwd_flops(), w.bwd_flops()
     bwd_alg = bwd_f  # the deterministic pass's recomputation of S and dP is not credited
-    value = world * (fwd_f + bwd_alg) / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, fwd_f + bwd_alg, ms_step)
     pk = peaks()
     peak_sust = pk["sustained"]
     fwd_tf = fwd_f / (per_kernel["fwd"] * 1e-3) / 1e12
@@ -352,11 +365,8 @@ def run_ours(args, w):
         e2.record(stream)
         torch.cuda.synchronize()
         e_ms = s2.elapsed_time(e2) / args.steps
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * (fwd_f + bwd_alg) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = slowest_rank(e_ms, dist, dev)
+        e2e = {"value": whole_job_tflops(world, fwd_f + bwd_alg, e_ms), "unit": "TFLOP/s",
                "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # the long-context forward-only workload, reported beside the step
@@ -384,7 +394,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, nrows, cores = time_oracle(w, inputs, 64)
+        v, dt, nrows, cores = time_oracle(w, inputs, 1024)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{nrows} query rows of {w.describe()} ({nrows // w.H} per head), "
                          f"each row's whole forward and backward share, fp64, {dt:.1f} s"}
