@@ -393,23 +393,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 //   TMEM [128b + 64, 128b + 128) buffer b: dP^T of tile i; then, for each
 //                                32-query half, P^T and dS^T packed over it
 //   TMEM [256, 384) dV, [384, 512) dK
-// The tensor core's order is
-//   S^T,dP^T(i) | dQ^T(i-2) | dV,dK(i-1) | S^T,dP^T(i+1) | dQ^T(i-1) | ...
-// so the scores of the next tile are always queued while the elementwise
-// warps work on the current one.  dQ^T(i-2) takes the S^T columns of tile
-// i-1 once those are consumed, and the dV/dK products that follow give the
-// four dQ warps time to drain it before S^T(i+1) reuses the buffer.  Q / dO (with
-// their LSE / Di rows) come through a three-stage ring; eight warps do the
-// elementwise work.  dV and dK take their A operands (P^T, dS^T) from TMEM,
-// so they read only dO or Q from shared memory; the tensor core's operand
-// bandwidth from shared memory (about 64 bytes per clock) is what bounds the
-// S^T / dP^T and dQ^T products, whose A comes from shared memory.
-// dQ is formed transposed, dQ^T = K^T dS^T (M = D), so
-// TMEM lane = column d and each atomic warp instruction covers 32
-// consecutive floats of one dQ row.  Because the tensor core completes
-// products in issue order, "S^T(i) is ready" also means dK(i-2) is done;
-// dQ^T(i-2), the other reader of dS^T buffer i & 1, is waited for apart.
-constexpr int kD128Threads = 448;  // warps 0-7 elementwise, 8-11 dQ, 12 producer, 13 MMA
+// Two warps issue the products.  The score warp issues S^T, dP^T(i) as soon
+// as buffer i & 1 is free; the gradient warp, once tile i's P^T / dS^T are
+// in TMEM, issues dQ^T(i-1) and then dV, dK(i).  Any stall of an issuing
+// thread (even a wait on a barrier that has already completed) leaves the
+// tensor core idle for a few hundred cycles while its next products travel
+// to it; with two issuers the other one's queued products fill that gap.
+// dQ^T(i-1) takes the S^T columns of tile i once those are consumed; the
+// four dQ warps drain it before S^T(i+2) reuses the buffer.  Q / dO (with
+// their LSE / Di rows) come through a three-stage ring, dS^T for dQ through
+// a three-stage shared buffer; eight warps do the elementwise work.  dV and
+// dK take their A operands (P^T, dS^T) from TMEM, so they read only dO or Q
+// from shared memory; the score and dQ^T products read both operands from
+// shared memory, which bounds them at 48 cycles per 128 x 64 x 16 product.
+// dQ is formed transposed, dQ^T = K^T dS^T (M = D), so TMEM lane = column d
+// and each atomic warp instruction covers 32 consecutive floats of one dQ row.
+constexpr int kD128Threads = 480;  // warps 0-7 elementwise, 8-11 dQ, 12 producer, 13-14 MMA
 constexpr int kQ64 = 64;
 
 struct Dkdv128Smem {
@@ -419,11 +418,11 @@ struct Dkdv128Smem {
   alignas(1024) uint8_t v[2 * kKBlock];
   alignas(1024) uint8_t q[3][2 * kQBlock];     // [stage][D block][64 queries][64 d]
   alignas(1024) uint8_t dO[3][2 * kQBlock];
-  alignas(1024) uint8_t dst[2][kKBlock];       // [buffer][128 keys][64 queries]
+  alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
-  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], dq_full[2], tmem_free[2];
-  uint64_t all_done, drain;
+  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], kv_done[2];
+  uint64_t dq_full[3], tmem_free[2], all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -453,15 +452,16 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     for (int i = 0; i < 3; ++i) {
       mbar_init(&s.qdo_full[i], 1);
       mbar_init(&s.qdo_empty[i], 1);
+      mbar_init(&s.dq_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
-      mbar_init(&s.dq_full[i], 1);
+      mbar_init(&s.kv_done[i], 1);
       mbar_init(&s.tmem_free[i], 128);
+      mbar_init(&s.drain[i], 1);
     }
     mbar_init(&s.all_done, 1);
-    mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -475,6 +475,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   const uint32_t tbase = s.tmem_base;
   const uint32_t tdV = tbase + 256, tdK = tbase + 384;
   volatile int* abort_flag = &s.abort_flag;
+  constexpr uint32_t ab = kBf16 ? 1u : 0u;
 
   if (warp == 12) {
     // ------------------------------------------------------------ producer
@@ -508,73 +509,85 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       }
     }
   } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score products
     if (lane == 0) {
-      constexpr uint32_t ab = kBf16 ? 1u : 0u;
       constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
-      constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
-      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);  // d x queries, over keys
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
-      // dQ^T(j) = K^T dS^T(j), issued once S^T(j + 1) is consumed, into the
-      // S^T columns of buffer (j + 1) & 1.
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int b = it & 1, st = it % 3;
+        // Buffer b last held tile it - 2, whose P^T / dS^T feed dV, dK(it - 2),
+        // and dQ^T(it - 3), which the dQ warps drain.
+        if (it >= 2 && !mbar_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) break;
+        if (kAtomicDq && it >= 3 &&
+            !mbar_wait(&s.tmem_free[b], ((it - 3) >> 1) & 1, p.err, abort_flag))
+          break;
+        if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+          const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+          tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
+                    desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+          const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+          tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
+                    desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s.s_full[b]);
+      }
+      tc_commit(&s.drain[0]);
+      int zero = 0;
+      mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ gradient products
+    if (lane == 0) {
+      constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
+      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);  // d x queries, over keys
+      const uint32_t k_addr = smem_u32(s.k);
+      bool ok = true;
+      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) & 1.
       auto issue_dq = [&](int j) {
-        const uint32_t dst_addr = smem_u32(s.dst[j & 1]);
+        const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           tc_mma_ss(tbase + ((j + 1) & 1) * 128,
                     desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
                     desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
                     kk > 0 ? 1u : 0u);
-        tc_commit(&s.dq_full[j & 1]);
+        tc_commit(&s.dq_full[j % 3]);
       };
-      for (int it = 0; ok && it <= n_it; ++it) {
-        if (it < n_it) {
-          const int b = it & 1, st = it % 3;
-          // Buffer b last held dQ^T(it - 3); it must be drained before reuse.
-          if (kAtomicDq && it >= 3 &&
-              !mbar_wait(&s.tmem_free[b], ((it - 3) >> 1) & 1, p.err, abort_flag))
-            break;
-          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
-                      desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
-                      desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&s.s_full[b]);
+      for (int it = 0; it < n_it; ++it) {
+        const int b = it & 1, st = it % 3;
+        if (!mbar_wait(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
         }
-        if (it >= 1) {
-          const int j = it - 1, bj = j & 1, st = j % 3;
-          if (!mbar_wait(&s.p_full[bj], (j >> 1) & 1, p.err, abort_flag)) break;
-          tc_fence_after();
-          // S^T(j) is consumed: dQ^T(j - 1) can take its columns.
-          if (kAtomicDq && j >= 1) issue_dq(j - 1);
-          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-          // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
+        tc_fence_after();
+        // S^T(it) is consumed: dQ^T(it - 1) can take its columns.  Their
+        // previous occupant, dQ^T(it - 3), was drained before S^T(it) was issued.
+        if (kAtomicDq && it >= 1) issue_dq(it - 1);
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+        // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
 #pragma unroll
-          for (int kk = 0; kk < kQ64 / 16; ++kk)
-            tc_mma_ts(tdV, tbase + bj * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                      desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
+        for (int kk = 0; kk < kQ64 / 16; ++kk)
+          tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                    desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
 #pragma unroll
-          for (int kk = 0; kk < kQ64 / 16; ++kk)
-            tc_mma_ts(tdK, tbase + bj * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
-                      desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&s.qdo_empty[st]);
-        }
+        for (int kk = 0; kk < kQ64 / 16; ++kk)
+          tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                    desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&s.qdo_empty[st]);
+        tc_commit(&s.kv_done[b]);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it.
@@ -585,10 +598,12 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           issue_dq(j);
         }
       }
+      // The score products all completed before the last P^T / dS^T existed,
+      // so this commit covers every product of the CTA.
       tc_commit(&s.all_done);
-      tc_commit(&s.drain);
+      tc_commit(&s.drain[1]);
       int zero = 0;
-      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+      mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain
@@ -597,7 +612,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       const int d = quad * 32 + lane;  // TMEM lane = column d of dQ
       const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
       for (int j = 0; j < n_it; ++j) {
-        if (!warp_wait(&s.dq_full[j & 1], (j >> 1) & 1, p.err, abort_flag)) break;
+        if (!warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const int b = (j + 1) & 1;  // dQ^T(j) sits in the S^T columns of tile j + 1
         uint32_t g[2][32];
@@ -627,8 +642,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1, st = it % 3;
       const int q0 = (it_begin + it) * kQ64;
-      // s_full also implies that the products of tile it - 2 (the last
-      // readers of dS^T buffer b) are complete.
+      // S^T(it) was issued after dV, dK(it - 2), the last readers of the
+      // P^T / dS^T columns of buffer b, had completed.
       if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) ||
           !warp_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) {
         ok = false;
@@ -666,12 +681,12 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
       tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32 + 16, dk);
       if (kAtomicDq) {
-        // dQ^T(it - 2) reads dS^T buffer b and is issued after S^T(it)
-        if (it >= 2 && !warp_wait(&s.dq_full[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) {
+        // dQ^T(it - 3) was the last reader of dS^T buffer it % 3
+        if (it >= 3 && !warp_wait(&s.dq_full[st], ((it - 3) / 3) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        store_row_chunk_sw128(s.dst[b], r, half, dk);
+        store_row_chunk_sw128(s.dst[st], r, half, dk);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
