@@ -422,7 +422,7 @@ struct Dkdv128Smem {
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
   uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], kv_done[2];
-  uint64_t dq_full[3], tmem_free[2], all_done, drain[2];
+  uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       mbar_init(&s.tmem_free[i], 128);
       mbar_init(&s.drain[i], 1);
     }
+    mbar_init(&s.ds_last, 256);
     mbar_init(&s.all_done, 1);
     s.abort_flag = 0;
     fence_barrier_init();
@@ -570,9 +571,6 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           break;
         }
         tc_fence_after();
-        // S^T(it) is consumed: dQ^T(it - 1) can take its columns.  Their
-        // previous occupant, dQ^T(it - 3), was drained before S^T(it) was issued.
-        if (kAtomicDq && it >= 1) issue_dq(it - 1);
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
         // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
 #pragma unroll
@@ -588,12 +586,20 @@ __global__ void __launch_bounds__(kD128Threads, 1)
                     (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&s.qdo_empty[st]);
         tc_commit(&s.kv_done[b]);
+        // S^T(it) is consumed: dQ^T(it - 1) can take its columns (their
+        // previous occupant, dQ^T(it - 3), was drained before S^T(it) was
+        // issued).  dS^T(it - 1) reached shared memory before P(it) was
+        // signalled.  dQ^T goes after dV, dK so that buffer b is released
+        // to the score warp as early as possible.
+        if (kAtomicDq && it >= 1) issue_dq(it - 1);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
-      // has left it.
+      // has left it and the last dS^T is in shared memory.
       if (ok && kAtomicDq && !*abort_flag) {
         const int j = n_it - 1;
-        if (j < 2 || mbar_wait(&s.tmem_free[(j + 1) & 1], ((j - 2) >> 1) & 1, p.err, abort_flag)) {
+        if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
+            (j < 2 ||
+             mbar_wait(&s.tmem_free[(j + 1) & 1], ((j - 2) >> 1) & 1, p.err, abort_flag))) {
           tc_fence_after();
           issue_dq(j);
         }
@@ -655,31 +661,65 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
       tmem_ld_wait();
       const bool diag = kCausal && (q0 < k0 + kTile);
-      const int key = k0 + r;
       uint32_t pk[16], dk[16];
+      if (!diag) {
+        // P = 2^(S * scale * log2 e - LSE2) and dS = P (dP - Di), two
+        // columns per packed instruction: the elementwise warps share
+        // their SM sub-partitions with the MMA-issuing warps, so every
+        // instruction saved here is issue time given back to the tensor core.
+        const uint64_t nsl2 = f32x2(-sl2, -sl2), neg1 = f32x2(-1.f, -1.f);
 #pragma unroll
-      for (int t = 0; t < 32; t += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
-        const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
-        const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pv[4], dsv[4];
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
-          if (diag && key > q0 + half * 32 + t + e) pe = 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
+          for (int h = 0; h < 2; ++h) {
+            const int e = t + 2 * h;
+            // -z = LSE2 - S * scale_log2
+            const float2 nz = split_f32x2(
+                fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
+                          h ? f32x2(l4.z, l4.w) : f32x2(l4.x, l4.y)));
+            const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
+            const uint64_t dd =
+                fma_f32x2(h ? f32x2(d4.z, d4.w) : f32x2(d4.x, d4.y), neg1,
+                          f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])));
+            const float2 ds = split_f32x2(mul_f32x2(f32x2(p0, p1), dd));
+            pk[e / 2] = pack2<kBf16>(p0, p1);
+            dk[e / 2] = pack2<kBf16>(ds.x, ds.y);
+          }
         }
-        pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
-        pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
-        dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
-        dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
+      } else {
+        // diagonal tile: key k0 + r sees query q only when q >= k0 + r
+        const int key = k0 + r;
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
+          const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
+            if (key > q0 + half * 32 + t + e) pe = 0.f;
+            pv[e] = pe;
+            dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
+          }
+          pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
+          pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
+          dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
+          dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
+        }
       }
       // P^T and dS^T over this warp's own 32 dP^T columns (already read):
       // P^T in the first 16, dS^T in the next 16.
       tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
       tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32 + 16, dk);
+      tmem_st_wait();
+      tc_fence_before();
+      // P(it) also publishes dS^T(it - 1), stored and fenced below in the
+      // previous iteration; dV, dK(it) need only the TMEM operands.
+      mbar_arrive(&s.p_full[b]);
       if (kAtomicDq) {
         // dQ^T(it - 3) was the last reader of dS^T buffer it % 3
         if (it >= 3 && !warp_wait(&s.dq_full[st], ((it - 3) / 3) & 1, p.err, abort_flag)) {
@@ -687,12 +727,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           break;
         }
         store_row_chunk_sw128(s.dst[st], r, half, dk);
+        fence_proxy_async_smem();
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&s.p_full[b]);
     }
+    if (kAtomicDq && ok) mbar_arrive(&s.ds_last);
 
     // ---------------------------------------------------------- epilogue
     const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
