@@ -276,16 +276,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         for (int c = 0; c < kTile; ++c)
           if (c > last) sv[c] = -INFINITY;
       }
-      // Row maximum with eight independent chains (short dependency depth).
+      // Row maximum: eight independent chains of three-input max.
       float mxs[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mxs[e] = sv[e];
 #pragma unroll
-      for (int c = 8; c < kTile; c += 8)
+      for (int c = 8; c < kTile; c += 16)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mxs[e] = fmaxf(mxs[e], sv[c + e]);
-      const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                             fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+        for (int e = 0; e < 8; ++e)
+          mxs[e] = c + 8 < kTile ? fmax3(mxs[e], sv[c + e], sv[c + 8 + e]) : fmaxf(mxs[e], sv[c + e]);
+      const float mx = fmax3(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], mxs[5]),
+                             fmaxf(mxs[6], mxs[7]));
       const float m_tile = pos_scale ? mx * sl2 : mx;
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + kRescaleThreshold;
@@ -313,22 +314,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
       }
       const float mneg = (m == -INFINITY) ? 0.f : -m;
-      float sums[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
+      // P = 2^(x * mult - m), two columns per packed FMA / add; the softmax
+      // warps share issue slots with the MMA warp, so fewer instructions
+      // here keep the tensor core fed.
+      const float mult = pos_scale ? sl2 : 1.f;
+      const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
+      uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float x0 = sv[h * 64 + 2 * c], x1 = sv[h * 64 + 2 * c + 1];
-          const float p0 = ex2_approx(pos_scale ? fmaf(x0, sl2, mneg) : x0 + mneg);
-          const float p1 = ex2_approx(pos_scale ? fmaf(x1, sl2, mneg) : x1 + mneg);
-          sums[(c & 1) * 2] += p0;
-          sums[(c & 1) * 2 + 1] += p1;
+          const float2 z = split_f32x2(
+              fma_f32x2(f32x2(sv[h * 64 + 2 * c], sv[h * 64 + 2 * c + 1]), mult2, mneg2));
+          const float p0 = ex2_approx(z.x), p1 = ex2_approx(z.y);
+          sums[c & 1] = add_f32x2(sums[c & 1], f32x2(p0, p1));
           pk[c] = pack2<kBf16>(p0, p1);
         }
         tmem_st32(tS + lane_off + h * 32, pk);
       }
-      l += (sums[0] + sums[1]) + (sums[2] + sums[3]);
+      const float2 s0 = split_f32x2(sums[0]), s1 = split_f32x2(sums[1]);
+      l += (s0.x + s0.y) + (s1.x + s1.y);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.p_full[t]);
