@@ -1,0 +1,128 @@
+"""flash_attn_func-style entry points with autograd.
+
+The argument list follows the FlashAttention interface described by the
+claire-chang.com introduction ([API]): q, k, v of shape
+(batch, seqlen, nheads, headdim), softmax_scale defaulting to 1/sqrt(headdim),
+causal, deterministic; and the packed variant taking one
+(batch, seqlen, 3, nheads, headdim) tensor.  Both run the library's kernels
+on the caller's tensors in place through the strided C ABI (fa_fwd_strided,
+fa_bwd_strided): no transposes or copies of Q, K, V.  Dropout, sliding
+windows and ALiBi are not provided; asking for them raises.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import fattn
+
+__all__ = ["flash_attn_func", "flash_attn_qkvpacked_func"]
+
+
+def _check_options(dropout_p, window_size, alibi_slopes):
+    if dropout_p:
+        raise NotImplementedError("dropout is not supported (dropout_p must be 0)")
+    if tuple(window_size) != (-1, -1):
+        raise NotImplementedError("sliding-window attention is not supported yet")
+    if alibi_slopes is not None:
+        raise NotImplementedError("ALiBi is not supported yet")
+
+
+def _bnhd(t) -> fattn.FaStrides:
+    return fattn.strides_of(t, "bnhd")
+
+
+def _grad_operand(g):
+    """The incoming gradient as the kernels need it: D contiguous, 16-byte
+    aligned rows.  Anything else is copied once (argument marshalling)."""
+    if g.stride(-1) != 1 or any(s % 8 for s in g.stride()[:-1]) or g.data_ptr() % 16:
+        g = g.contiguous()
+    return g
+
+
+def _layout(q, k, v, o, do=None, dq=None, dk=None, dv=None) -> fattn.FaLayout:
+    z = fattn.FaStrides(0, 0, 0)
+    return fattn.FaLayout(_bnhd(q), _bnhd(k), _bnhd(v), _bnhd(o),
+                          _bnhd(do) if do is not None else z, _bnhd(dq) if dq is not None else z,
+                          _bnhd(dk) if dk is not None else z, _bnhd(dv) if dv is not None else z)
+
+
+def _forward(q, k, v, scale, causal):
+    B, N, H, D = (int(x) for x in q.shape)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same (batch, seqlen, nheads, headdim) shape")
+    o = torch.empty((B, N, H, D), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fattn.fa_fwd_strided(q, k, v, o, lse, _layout(q, k, v, o), B, H, N, D, scale, causal)
+    return o, lse
+
+
+def _backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, deterministic):
+    B, N, H, D = (int(x) for x in q.shape)
+    fattn.fa_bwd_strided(q, k, v, o, lse, do, dq, dk, dv, _layout(q, k, v, o, do, dq, dk, dv),
+                         B, H, N, D, scale, causal, deterministic)
+
+
+class _FlashAttn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal, deterministic):
+        o, lse = _forward(q, k, v, scale, causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal, ctx.deterministic = scale, causal, deterministic
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
+                  ctx.deterministic)
+        return dq, dk, dv, None, None, None
+
+
+class _FlashAttnQKVPacked(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, qkv, scale, causal, deterministic):
+        q, k, v = qkv.unbind(dim=2)
+        o, lse = _forward(q, k, v, scale, causal)
+        ctx.save_for_backward(qkv, o, lse)
+        ctx.scale, ctx.causal, ctx.deterministic = scale, causal, deterministic
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        qkv, o, lse = ctx.saved_tensors
+        q, k, v = qkv.unbind(dim=2)
+        dqkv = torch.empty_like(qkv)
+        dq, dk, dv = dqkv.unbind(dim=2)
+        _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
+                  ctx.deterministic)
+        return dqkv, None, None, None
+
+
+def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=False,
+                    window_size=(-1, -1), alibi_slopes=None, deterministic=False,
+                    return_lse=False):
+    """Exact attention of q, k, v shaped (batch, seqlen, nheads, headdim),
+    bf16 or fp16 CUDA tensors with headdim 64 or 128 contiguous.  Returns the
+    output in the same shape (and the fp32 (batch, nheads, seqlen) log-sum-exp
+    of the scaled scores when return_lse).  Differentiable in q, k, v;
+    deterministic selects the two-pass dQ backward."""
+    _check_options(dropout_p, window_size, alibi_slopes)
+    scale = q.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
+    o, lse = _FlashAttn.apply(q, k, v, scale, bool(causal), bool(deterministic))
+    return (o, lse) if return_lse else o
+
+
+def flash_attn_qkvpacked_func(qkv, dropout_p=0.0, softmax_scale=None, causal=False,
+                              window_size=(-1, -1), alibi_slopes=None, deterministic=False,
+                              return_lse=False):
+    """flash_attn_func on one packed (batch, seqlen, 3, nheads, headdim)
+    tensor; its gradient comes back in the same packed layout."""
+    _check_options(dropout_p, window_size, alibi_slopes)
+    if qkv.dim() != 5 or qkv.shape[2] != 3:
+        raise ValueError("expected qkv of shape (batch, seqlen, 3, nheads, headdim)")
+    scale = qkv.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
+    o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), bool(deterministic))
+    return (o, lse) if return_lse else o

@@ -72,14 +72,37 @@ fa_status check_ws(const Shape& s, int deterministic, const void* ws, size_t byt
   return FA_OK;
 }
 
-bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype, int box_rows = kTile) {
-  return make_tmap_3d(m, base,
-                      dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                      2, static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.N),
-                      static_cast<uint64_t>(s.BH()), static_cast<uint64_t>(s.D),
-                      static_cast<uint64_t>(s.N) * s.D, 64, static_cast<uint32_t>(box_rows),
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+// Element strides of every operand of one call (D contiguous).
+struct Layout {
+  RowStrides q, k, v, o, dO, dq, dk, dv;
+};
+
+Layout contiguous_layout(const Shape& s) {
+  const RowStrides c{static_cast<long long>(s.H) * s.N * s.D, static_cast<long long>(s.N) * s.D,
+                     static_cast<long long>(s.D)};
+  return Layout{c, c, c, c, c, c, c, c};
+}
+
+Layout from_abi(const fa_layout& l) {
+  auto r = [](const fa_strides& x) { return RowStrides{x.batch, x.head, x.seq}; };
+  return Layout{r(l.q), r(l.k), r(l.v), r(l.o), r(l.dO), r(l.dq), r(l.dk), r(l.dv)};
+}
+
+// TMA wants 16-byte multiples; every element of the operand must lie below
+// 2^40 bytes from its base.
+fa_status check_strides(const Shape& s, const RowStrides& r) {
+  const long long st[3] = {r.batch, r.head, r.seq};
+  for (long long x : st)
+    if (x < 0 || (x & 7) != 0) return FA_ERR_INVALID_ARG;
+  const double last = static_cast<double>(s.B - 1) * r.batch + static_cast<double>(s.H - 1) * r.head +
+                      static_cast<double>(s.N - 1) * r.seq + s.D;
+  return last * 2.0 < 1099511627776.0 ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype, const RowStrides& r,
+              int box_rows = kTile) {
+  return operand_map(m, base, dtype == FA_BF16, s.B, s.H, s.N, s.D, r.batch, r.head, r.seq,
+                     box_rows);
 }
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
@@ -88,16 +111,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Everything the dK/dV and dQ kernels share.
 fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void* v,
-                          const void* dO, void* dq, void* dk, void* dv, const Shape& s, float scale,
-                          int causal, int dtype, int deterministic, void* ws) {
+                          const void* dO, void* dq, void* dk, void* dv, const Shape& s,
+                          const Layout& L, float scale, int causal, int dtype, int deterministic,
+                          void* ws) {
   *a = BwdLaunch{};
-  if (!tile_map(&a->map_q, q, s, dtype) || !tile_map(&a->map_k, k, s, dtype) ||
-      !tile_map(&a->map_v, v, s, dtype) || !tile_map(&a->map_do, dO, s, dtype) ||
-      !tile_map(&a->map_q64, q, s, dtype, 64) || !tile_map(&a->map_do64, dO, s, dtype, 64))
+  if (!tile_map(&a->map_q, q, s, dtype, L.q) || !tile_map(&a->map_k, k, s, dtype, L.k) ||
+      !tile_map(&a->map_v, v, s, dtype, L.v) || !tile_map(&a->map_do, dO, s, dtype, L.dO) ||
+      !tile_map(&a->map_q64, q, s, dtype, L.q, 64) ||
+      !tile_map(&a->map_do64, dO, s, dtype, L.dO, 64))
     return FA_ERR_CUDA;
-  if (dq && !tile_map(&a->map_dq, dq, s, dtype)) return FA_ERR_CUDA;
-  if (dk && !tile_map(&a->map_dk, dk, s, dtype)) return FA_ERR_CUDA;
-  if (dv && !tile_map(&a->map_dv, dv, s, dtype)) return FA_ERR_CUDA;
+  if (dq && !tile_map(&a->map_dq, dq, s, dtype, L.dq)) return FA_ERR_CUDA;
+  if (dk && !tile_map(&a->map_dk, dk, s, dtype, L.dk)) return FA_ERR_CUDA;
+  if (dv && !tile_map(&a->map_dv, dv, s, dtype, L.dv)) return FA_ERR_CUDA;
   const WsLayout w = ws_layout(s, deterministic);
   auto* base = static_cast<uint8_t*>(ws);
   a->lse = reinterpret_cast<const float*>(base + w.lse2);
@@ -106,6 +131,7 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
   a->N = s.N;
   a->BH = static_cast<int>(s.BH());
   a->D = s.D;
+  a->H = s.H;
   a->scale = scale;
   a->scale_log2 = scale * kLog2e;
   a->causal = causal ? 1 : 0;
@@ -125,7 +151,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 1; }
+int fa_abi_version(void) { return 2; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -138,28 +164,85 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                 int N, int D, float scale, int causal, fa_dtype dtype, void* stream) {
-  const Shape s{B, H, N, D};
+}  // extern "C"
+
+namespace {
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                   const Shape& s, const Layout& L, float scale, int causal, int dtype,
+                   void* stream) {
   fa_status st = check_shape(s, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
+  for (const RowStrides* r : {&L.q, &L.k, &L.v, &L.o})
+    if ((st = check_strides(s, *r)) != FA_OK) return st;
   FwdLaunch a{};
-  if (!tile_map(&a.map_q, q, s, dtype) || !tile_map(&a.map_k, k, s, dtype) ||
-      !tile_map(&a.map_v, v, s, dtype) || !tile_map(&a.map_o, o, s, dtype))
+  if (!tile_map(&a.map_q, q, s, dtype, L.q) || !tile_map(&a.map_k, k, s, dtype, L.k) ||
+      !tile_map(&a.map_v, v, s, dtype, L.v) || !tile_map(&a.map_o, o, s, dtype, L.o))
     return FA_ERR_CUDA;
   a.lse = lse;
-  a.N = N;
+  a.N = s.N;
   a.BH = static_cast<int>(s.BH());
-  a.D = D;
+  a.D = s.D;
+  a.H = s.H;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
   a.bf16 = dtype == FA_BF16 ? 1 : 0;
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
   return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, const Shape& s, const Layout& L,
+                   float scale, int causal, int dtype, int deterministic, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  fa_status st = check_shape(s, dtype);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  for (const RowStrides* r : {&L.q, &L.k, &L.v, &L.o, &L.dO, &L.dq, &L.dk, &L.dv})
+    if ((st = check_strides(s, *r)) != FA_OK) return st;
+  if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
+  // Build every descriptor before enqueueing anything.
+  BwdLaunch a;
+  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, dk, dv, s, L, scale, causal, dtype,
+                            deterministic, workspace)) != FA_OK)
+    return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const WsLayout w = ws_layout(s, deterministic);
+  auto* base = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_bwd_preprocess(o, L.o, dO, L.dO, lse,
+                                        reinterpret_cast<float*>(base + w.lse2),
+                                        reinterpret_cast<float*>(base + w.di), a.dq_accum, s.N,
+                                        s.H, s.BH(), s.D, dtype == FA_BF16, cs);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if ((e = launch_bwd_dkdv(a, cs)) != cudaSuccess) return FA_ERR_CUDA;
+  if (deterministic) return from_cuda(launch_bwd_dq(a, cs));
+  return from_cuda(launch_dq_convert(a.dq_accum, dq, L.dq, s.N, s.H, s.BH(), s.D, scale,
+                                     dtype == FA_BF16, cs));
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int D, float scale, int causal, fa_dtype dtype, void* stream) {
+  const Shape s{B, H, N, D};
+  return fwd_impl(q, k, v, o, lse, s, contiguous_layout(s), scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int D, const fa_layout* layout, float scale, int causal,
+                         fa_dtype dtype, void* stream) {
+  if (!layout) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, Shape{B, H, N, D}, from_abi(*layout), scale, causal, dtype,
+                  stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic) {
@@ -178,9 +261,11 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, const float* lse, int
   if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
   const WsLayout w = ws_layout(s, deterministic);
   auto* base = static_cast<uint8_t*>(workspace);
+  const Layout L = contiguous_layout(s);
   return from_cuda(launch_bwd_preprocess(
-      o, dO, lse, reinterpret_cast<float*>(base + w.lse2), reinterpret_cast<float*>(base + w.di),
-      deterministic ? nullptr : reinterpret_cast<float*>(base + w.dq), N, s.BH(), D,
+      o, L.o, dO, L.dO, lse, reinterpret_cast<float*>(base + w.lse2),
+      reinterpret_cast<float*>(base + w.di),
+      deterministic ? nullptr : reinterpret_cast<float*>(base + w.dq), N, H, s.BH(), D,
       dtype == FA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
@@ -197,8 +282,8 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
     return FA_ERR_INVALID_ARG;
   if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
-  if ((st = make_bwd_launch(&a, q, k, v, dO, nullptr, dk, dv, s, scale, causal, dtype,
-                            deterministic, workspace)) != FA_OK)
+  if ((st = make_bwd_launch(&a, q, k, v, dO, nullptr, dk, dv, s, contiguous_layout(s), scale,
+                            causal, dtype, deterministic, workspace)) != FA_OK)
     return st;
   return from_cuda(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
 }
@@ -214,8 +299,8 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     return FA_ERR_INVALID_ARG;
   if ((st = check_ws(s, 1, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
-  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, nullptr, nullptr, s, scale, causal, dtype, 1,
-                            workspace)) != FA_OK)
+  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, nullptr, nullptr, s, contiguous_layout(s),
+                            scale, causal, dtype, 1, workspace)) != FA_OK)
     return st;
   return from_cuda(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
 }
@@ -230,8 +315,8 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int D, float scale, f
   if ((st = check_ws(s, 0, workspace, workspace_bytes)) != FA_OK) return st;
   const WsLayout w = ws_layout(s, 0);
   const float* acc = reinterpret_cast<const float*>(static_cast<uint8_t*>(workspace) + w.dq);
-  return from_cuda(launch_dq_convert(acc, dq, s.BH() * s.N * s.D, scale, dtype == FA_BF16,
-                                     static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_dq_convert(acc, dq, contiguous_layout(s).dq, N, H, s.BH(), D, scale,
+                                     dtype == FA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -239,29 +324,18 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, fa_dtype dtype, int deterministic, void* workspace,
                  size_t workspace_bytes, void* stream) {
   const Shape s{B, H, N, D};
-  fa_status st = check_shape(s, dtype);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_INVALID_ARG;
-  if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
-  // Build every descriptor before enqueueing anything.
-  BwdLaunch a;
-  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, dk, dv, s, scale, causal, dtype, deterministic,
-                            workspace)) != FA_OK)
-    return st;
-  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const WsLayout w = ws_layout(s, deterministic);
-  auto* base = static_cast<uint8_t*>(workspace);
-  cudaError_t e = launch_bwd_preprocess(
-      o, dO, lse, reinterpret_cast<float*>(base + w.lse2), reinterpret_cast<float*>(base + w.di),
-      a.dq_accum, N, s.BH(), D, dtype == FA_BF16, cs);
-  if (e != cudaSuccess) return FA_ERR_CUDA;
-  if ((e = launch_bwd_dkdv(a, cs)) != cudaSuccess) return FA_ERR_CUDA;
-  if (deterministic) return from_cuda(launch_bwd_dq(a, cs));
-  return from_cuda(
-      launch_dq_convert(a.dq_accum, dq, s.BH() * s.N * s.D, scale, dtype == FA_BF16, cs));
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, s, contiguous_layout(s), scale, causal, dtype,
+                  deterministic, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int D, const fa_layout* layout, float scale, int causal,
+                         fa_dtype dtype, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!layout) return FA_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Shape{B, H, N, D}, from_abi(*layout), scale,
+                  causal, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_device_error(void* stream, int* code) {

@@ -73,12 +73,14 @@ __device__ __forceinline__ void store_row_chunk_sw128(uint8_t* tile, int r, int 
 // One group of D/8 threads per row; each thread handles 8 columns.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __restrict__ o,
+                                                             RowStrides so,
                                                              const uint16_t* __restrict__ dO,
+                                                             RowStrides sdo,
                                                              const float* __restrict__ lse,
                                                              float* __restrict__ lse2,
                                                              float* __restrict__ di,
                                                              float* __restrict__ dq_accum, int N,
-                                                             int Npad, long long BH) {
+                                                             int Npad, int H, long long BH) {
   constexpr int G = D / 8;  // threads per row
   const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long prow = gtid / G;  // padded row index over BH * Npad
@@ -88,14 +90,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
   const int n = static_cast<int>(prow % Npad);
   float acc = 0.f;
   if (n < N) {
+    const long long b = bh / H, h = bh % H;
     const long long row = bh * N + n;
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + part * 8);
+    const uint4 a = *reinterpret_cast<const uint4*>(o + b * so.batch + h * so.head + n * so.seq +
+                                                    part * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(dO + b * sdo.batch + h * sdo.head +
+                                                    n * sdo.seq + part * 8);
     const uint32_t* aa = reinterpret_cast<const uint32_t*>(&a);
-    const uint32_t* bb = reinterpret_cast<const uint32_t*>(&b);
+    const uint32_t* gg = reinterpret_cast<const uint32_t*>(&g);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const float2 x = unpack2<kBf16>(aa[t]), y = unpack2<kBf16>(bb[t]);
+      const float2 x = unpack2<kBf16>(aa[t]), y = unpack2<kBf16>(gg[t]);
       acc = fmaf(x.x, y.x, acc);
       acc = fmaf(x.y, y.y, acc);
     }
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   const int Npad = n_tiles * kTile;
   // Head-major; key tiles near the start see the most queries and go first.
   const int bh = static_cast<int>(blockIdx.x / n_tiles);
+  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int kt = static_cast<int>(blockIdx.x % n_tiles);
   const int k0 = kt * kTile;
   const int it_begin = kCausal ? kt : 0;
@@ -178,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     if (lane == 0) {
       mbar_arrive_expect_tx(&s.kv_full, 2 * Smem::kTileBytes);
       for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-        tma_load_3d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.kv_full, kb * 64, k0, bh);
-        tma_load_3d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.kv_full, kb * 64, k0, bh);
+        tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.kv_full, kb * 64, k0, hh, bb);
+        tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -187,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (it >= 1 && !mbar_wait(&s.qdo_empty, (it - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes + 2 * kTile * 4);
         for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-          tma_load_3d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, bh);
-          tma_load_3d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, bh);
+          tma_load_4d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, hh, bb);
+          tma_load_4d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, hh, bb);
         }
         const long long off = static_cast<long long>(bh) * Npad + q0;
         bulk_load(s.lse2, p.lse + off, kTile * 4, &s.qdo_full);
@@ -366,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       named_bar_sync(1, 128);
       if (tid == 0) {
         for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-          tma_store_3d(&p.map_dv, s.dO + kb * Smem::kBlockBytes, kb * 64, k0, bh);
-          tma_store_3d(&p.map_dk, s.q + kb * Smem::kBlockBytes, kb * 64, k0, bh);
+          tma_store_4d(&p.map_dv, s.dO + kb * Smem::kBlockBytes, kb * 64, k0, hh, bb);
+          tma_store_4d(&p.map_dk, s.q + kb * Smem::kBlockBytes, kb * 64, k0, hh, bb);
         }
         tma_store_commit();
         tma_store_wait_all();
@@ -442,6 +448,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   // Head-major order, longest key tiles first within a head: the CTAs in
   // flight share one head's Q, dO and dQ accumulator in L2.
   const int bh = static_cast<int>(blockIdx.x / n_kt);
+  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int kt = static_cast<int>(blockIdx.x % n_kt);
   const int k0 = kt * kTile;
   const int it_begin = kCausal ? 2 * kt : 0;  // first 64-row query tile that sees a key here
@@ -483,8 +490,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(&s.kv_full, 4 * Smem::kKBlock);
       for (int kb = 0; kb < 2; ++kb) {
-        tma_load_3d(s.k + kb * Smem::kKBlock, &p.map_k, &s.kv_full, kb * 64, k0, bh);
-        tma_load_3d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, bh);
+        tma_load_4d(s.k + kb * Smem::kKBlock, &p.map_k, &s.kv_full, kb * 64, k0, hh, bb);
+        tma_load_4d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -493,9 +500,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         const int q0 = (it_begin + it) * kQ64;
         mbar_arrive_expect_tx(&s.qdo_full[st], 4 * Smem::kQBlock + 2 * kQ64 * 4);
         for (int kb = 0; kb < 2; ++kb) {
-          tma_load_3d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, bh);
-          tma_load_3d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0,
-                      bh);
+          tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, hh, bb);
+          tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0, hh, bb);
         }
         const long long off = static_cast<long long>(bh) * Npad + q0;
         bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
@@ -759,8 +765,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       named_bar_sync(1, 256);
       if (tid == 0) {
         for (int kb = 0; kb < 2; ++kb) {
-          tma_store_3d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, bh);
-          tma_store_3d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, bh);
+          tma_store_4d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
+          tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
         }
         tma_store_commit();
         tma_store_wait_all();
@@ -805,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const int Npad = n_tiles * kTile;
   // Head-major; under the causal mask the longest query tiles go first.
   const int bh = static_cast<int>(blockIdx.x / n_tiles);
+  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int qt = kCausal ? n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles)
                          : static_cast<int>(blockIdx.x % n_tiles);
   const int q0 = qt * kTile;
@@ -838,20 +845,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     if (lane == 0) {
       mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes);
       for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-        tma_load_3d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, bh);
-        tma_load_3d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, bh);
+        tma_load_4d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, hh, bb);
+        tma_load_4d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, hh, bb);
       }
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         if (j >= 1 && !mbar_wait(&s.k_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_3d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, j * kTile, bh);
+          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, j * kTile, hh, bb);
         issued = 2 * j + 1;
         if (j >= 1 && !mbar_wait(&s.v_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.v_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_3d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, j * kTile, bh);
+          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, j * kTile, hh, bb);
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
@@ -969,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       named_bar_sync(1, 128);
       if (tid == 0) {
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_store_3d(&p.map_dq, s.q + kb * Smem::kBlockBytes, kb * 64, q0, bh);
+          tma_store_4d(&p.map_dq, s.q + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
         tma_store_commit();
         tma_store_wait_all();
       }
@@ -987,11 +994,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // dQ convert
 // ---------------------------------------------------------------------------
+// acc is [BH][N][D] fp32; dq gets scale * acc in the caller's layout.  One
+// thread per 8 consecutive elements of a row.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         uint16_t* __restrict__ dq,
-                                                         long long n8, float scale) {
+                                                         uint16_t* __restrict__ dq, RowStrides sdq,
+                                                         int N, int H, int D, long long n8,
+                                                         float scale) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int g = D / 8;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
        t += stride) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
@@ -1001,7 +1012,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     o.y = pack2<kBf16>(a.z * scale, a.w * scale);
     o.z = pack2<kBf16>(b.x * scale, b.y * scale);
     o.w = pack2<kBf16>(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4*>(dq)[t] = o;
+    const long long row = t / g;  // over BH * N
+    const long long bh = row / N, n = row % N;
+    *reinterpret_cast<uint4*>(dq + (bh / H) * sdq.batch + (bh % H) * sdq.head + n * sdq.seq +
+                              (t % g) * 8) = o;
   }
 }
 
@@ -1082,9 +1096,9 @@ cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* lse2,
-                                  float* di, float* dq_accum, int N, long long BH, int D, int bf16,
-                                  cudaStream_t st) {
+cudaError_t launch_bwd_preprocess(const void* o, RowStrides so, const void* dO, RowStrides sdo,
+                                  const float* lse, float* lse2, float* di, float* dq_accum, int N,
+                                  int H, long long BH, int D, int bf16, cudaStream_t st) {
   const int Npad = (N + kTile - 1) / kTile * kTile;
   const long long threads = BH * Npad * (D / 8);
   const long long blocks = (threads + 255) / 256;
@@ -1093,11 +1107,11 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* ls
   const auto* d16 = static_cast<const uint16_t*>(dO);
   const unsigned g = static_cast<unsigned>(blocks);
   if (D == 64) {
-    if (bf16) bwd_preprocess_kernel<64, true><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
-    else bwd_preprocess_kernel<64, false><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+    if (bf16) bwd_preprocess_kernel<64, true><<<g, 256, 0, st>>>(o16, so, d16, sdo, lse, lse2, di, dq_accum, N, Npad, H, BH);
+    else bwd_preprocess_kernel<64, false><<<g, 256, 0, st>>>(o16, so, d16, sdo, lse, lse2, di, dq_accum, N, Npad, H, BH);
   } else {
-    if (bf16) bwd_preprocess_kernel<128, true><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
-    else bwd_preprocess_kernel<128, false><<<g, 256, 0, st>>>(o16, d16, lse, lse2, di, dq_accum, N, Npad, BH);
+    if (bf16) bwd_preprocess_kernel<128, true><<<g, 256, 0, st>>>(o16, so, d16, sdo, lse, lse2, di, dq_accum, N, Npad, H, BH);
+    else bwd_preprocess_kernel<128, false><<<g, 256, 0, st>>>(o16, so, d16, sdo, lse, lse2, di, dq_accum, N, Npad, H, BH);
   }
   return cudaGetLastError();
 }
@@ -1116,16 +1130,18 @@ cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t st) {
   return a.causal ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
 }
 
-cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale, int bf16,
-                              cudaStream_t st) {
-  const long long n8 = n / 8;
+cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N, int H,
+                              long long BH, int D, float scale, int bf16, cudaStream_t st) {
+  const long long n8 = BH * N * D / 8;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
+  auto* d16 = static_cast<uint16_t*>(dq);
+  const unsigned g = static_cast<unsigned>(blocks);
   if (bf16)
-    dq_convert_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<uint16_t*>(dq), n8, scale);
+    dq_convert_kernel<true><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, D, n8, scale);
   else
-    dq_convert_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<uint16_t*>(dq), n8, scale);
+    dq_convert_kernel<false><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, D, n8, scale);
   return cudaGetLastError();
 }
 

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   const int n_q_tiles = (p.N + kTile - 1) / kTile;
   const int n_pairs = (n_q_tiles + 1) / 2;
   const int bh = static_cast<int>(blockIdx.x / n_pairs);
+  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int pt = kCausal ? n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs)
                          : static_cast<int>(blockIdx.x % n_pairs);
   const int n_kv = (p.N + kTile - 1) / kTile;
@@ -129,8 +130,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       mbar_arrive_expect_tx(&s.q_full, n_q_here * Smem::kTileBytes);
       for (int t = 0; t < n_q_here; ++t)
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_3d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full, kb * 64,
-                      (2 * pt + t) * kTile, bh);
+          tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full, kb * 64,
+                      (2 * pt + t) * kTile, hh, bb);
       int issued = 0;
       for (int j = 0; j < n_max; ++j) {
         const int st = j & 1;
@@ -138,16 +139,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         if (j >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_3d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st], kb * 64,
-                      j * kTile, bh);
+          tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st], kb * 64,
+                      j * kTile, hh, bb);
         if (j >= 2 && !mbar_wait(&s.v_empty[st], (u - 1) & 1, p.err, abort_flag)) {
           issued = j * 2 + 1;
           break;
         }
         mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_3d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
-                      j * kTile, bh);
+          tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
+                      j * kTile, hh, bb);
         issued = j * 2 + 2;
       }
       if (*abort_flag) {
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         named_bar_sync(1 + t, 128);
         if (r == 0) {
           for (int kb = 0; kb < Smem::kBlocks; ++kb)
-            tma_store_3d(&p.map_o, stage + kb * Smem::kBlockBytes, kb * 64, q0, bh);
+            tma_store_4d(&p.map_o, stage + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
           tma_store_commit();
           tma_store_wait_all();
         }

@@ -11,36 +11,43 @@ namespace fa {
 
 constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 
+// Tensor maps are 4-D {D, N, H, B} over the caller's strides (D contiguous);
+// kernels address (batch, head) slice bh as head bh % H, batch bh / H.
 struct FwdLaunch {
-  CUtensorMap map_q, map_k, map_v, map_o;  // [BH][N][D], box 64 x 128, 128B swizzle
+  CUtensorMap map_q, map_k, map_v, map_o;  // box 64 x 128 x 1 x 1, 128B swizzle
   float* lse;                               // [BH][N]
-  int N, BH, D;
+  int N, BH, D, H;
   float scale_log2;                         // scale * log2(e)
   int causal, bf16;
   uint32_t* err;
 };
 
 struct BwdLaunch {
-  CUtensorMap map_q, map_k, map_v, map_do;  // [BH][N][D], box 64 x 128
+  CUtensorMap map_q, map_k, map_v, map_do;  // box 64 x 128 x 1 x 1
   CUtensorMap map_dq, map_dk, map_dv;       // outputs, same geometry
-  CUtensorMap map_q64, map_do64;            // Q and dO again, box 64 x 64
+  CUtensorMap map_q64, map_do64;            // Q and dO again, box 64 x 64 x 1 x 1
   const float* lse;                         // [BH][Npad] LSE * log2(e), +inf padding
   const float* di;                          // [BH][Npad] rowsum(dO * O), 0 padding
   float* dq_accum;                          // [BH][N][D] or nullptr
-  int N, BH, D;
+  int N, BH, D, H;
   float scale, scale_log2;
   int causal, bf16;
   uint32_t* err;
 };
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
-cudaError_t launch_bwd_preprocess(const void* o, const void* dO, const float* lse, float* lse2,
-                                  float* di, float* dq_accum, int N, long long BH, int D, int bf16,
-                                  cudaStream_t s);
+// Element strides of one [B, H, N, D] operand (D contiguous).
+struct RowStrides {
+  long long batch, head, seq;
+};
+
+cudaError_t launch_bwd_preprocess(const void* o, RowStrides so, const void* dO, RowStrides sdo,
+                                  const float* lse, float* lse2, float* di, float* dq_accum, int N,
+                                  int H, long long BH, int D, int bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t s);
-cudaError_t launch_dq_convert(const float* acc, void* dq, long long n, float scale, int bf16,
-                              cudaStream_t s);
+cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N, int H,
+                              long long BH, int D, float scale, int bf16, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 // Device address of the error word bounded waits write (current device), or

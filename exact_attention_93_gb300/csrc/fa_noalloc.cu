@@ -49,15 +49,11 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool tile_map(CUtensorMap* m, const void* base, int N, long long BH, int D, int dtype,
+// Contiguous [B, H, N, D] operand.
+bool tile_map(CUtensorMap* m, const void* base, int B, int H, int N, int D, int dtype,
               int box_rows = kTile) {
-  return make_tmap_3d(m, base,
-                      dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                      2, static_cast<uint64_t>(D), static_cast<uint64_t>(N),
-                      static_cast<uint64_t>(BH), static_cast<uint64_t>(D),
-                      static_cast<uint64_t>(N) * D, 64, static_cast<uint32_t>(box_rows),
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  return operand_map(m, base, dtype == FA_BF16, B, H, N, D, static_cast<long long>(H) * N * D,
+                     static_cast<long long>(N) * D, D, box_rows);
 }
 
 }  // namespace
@@ -89,11 +85,12 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (!scratch || !err) return FA_ERR_CUDA;
 
   BwdLaunch a{};
-  if (!tile_map(&a.map_q, q, N, BH, D, dtype) || !tile_map(&a.map_k, k, N, BH, D, dtype) ||
-      !tile_map(&a.map_v, v, N, BH, D, dtype) || !tile_map(&a.map_do, dO, N, BH, D, dtype) ||
-      !tile_map(&a.map_dq, dq, N, BH, D, dtype) || !tile_map(&a.map_dk, dk, N, BH, D, dtype) ||
-      !tile_map(&a.map_dv, dv, N, BH, D, dtype) || !tile_map(&a.map_q64, q, N, BH, D, dtype, 64) ||
-      !tile_map(&a.map_do64, dO, N, BH, D, dtype, 64))
+  if (!tile_map(&a.map_q, q, B, H, N, D, dtype) || !tile_map(&a.map_k, k, B, H, N, D, dtype) ||
+      !tile_map(&a.map_v, v, B, H, N, D, dtype) || !tile_map(&a.map_do, dO, B, H, N, D, dtype) ||
+      !tile_map(&a.map_dq, dq, B, H, N, D, dtype) || !tile_map(&a.map_dk, dk, B, H, N, D, dtype) ||
+      !tile_map(&a.map_dv, dv, B, H, N, D, dtype) ||
+      !tile_map(&a.map_q64, q, B, H, N, D, dtype, 64) ||
+      !tile_map(&a.map_do64, dO, B, H, N, D, dtype, 64))
     return FA_ERR_CUDA;
   float* lse2 = reinterpret_cast<float*>(scratch);
   float* di = reinterpret_cast<float*>(scratch + di_off);
@@ -103,6 +100,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   a.N = N;
   a.BH = static_cast<int>(BH);
   a.D = D;
+  a.H = H;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal ? 1 : 0;
@@ -112,7 +110,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   // The preprocess rewrites every scratch entry the later kernels read
   // (padding rows included), so the previous call's contents never leak in.
-  if (launch_bwd_preprocess(o, dO, lse, lse2, di, nullptr, N, BH, D, a.bf16, cs) != cudaSuccess)
+  const RowStrides rows_c{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D};
+  if (launch_bwd_preprocess(o, rows_c, dO, rows_c, lse, lse2, di, nullptr, N, H, BH, D, a.bf16,
+                            cs) != cudaSuccess)
     return FA_ERR_CUDA;
   if (launch_bwd_dkdv(a, cs) != cudaSuccess) return FA_ERR_CUDA;
   return launch_bwd_dq(a, cs) == cudaSuccess ? FA_OK : FA_ERR_CUDA;

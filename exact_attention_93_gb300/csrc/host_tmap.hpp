@@ -48,4 +48,39 @@ inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS;
 }
 
+// A [batch][head][rows][inner] tensor of 16-bit elements with arbitrary
+// element strides for rows, heads and batches (inner contiguous).  Boxes are
+// box_inner x box_rows x 1 x 1; out-of-range rows read as zero and are not
+// written.  Returns false when the driver rejects the map (alignment, sizes).
+inline bool make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         uint64_t inner, uint64_t rows, uint64_t heads, uint64_t batches,
+                         uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride,
+                         uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  constexpr uint64_t kElem = 2;
+  cuuint64_t dims[4] = {inner, rows, heads, batches};
+  cuuint64_t strides[3] = {row_stride * kElem, head_stride * kElem, batch_stride * kElem};
+  cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The map every tile kernel uses for a [B, H, N, D] operand: 64-column blocks
+// (128 bytes, 128-byte swizzle) of box_rows rows.
+inline bool operand_map(CUtensorMap* map, const void* base, bool bf16, int B, int H, int N, int D,
+                        long long batch_stride, long long head_stride, long long seq_stride,
+                        int box_rows) {
+  return make_tmap_4d(map, base,
+                      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      static_cast<uint64_t>(D), static_cast<uint64_t>(N),
+                      static_cast<uint64_t>(H), static_cast<uint64_t>(B),
+                      static_cast<uint64_t>(seq_stride), static_cast<uint64_t>(head_stride),
+                      static_cast<uint64_t>(batch_stride), 64, static_cast<uint32_t>(box_rows),
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace fa

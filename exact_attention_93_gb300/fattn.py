@@ -24,6 +24,17 @@ _lock = threading.Lock()
 _lib = None
 
 
+class FaStrides(ctypes.Structure):
+    """fa_strides: element strides (batch, head, seq) of one operand."""
+    _fields_ = [("batch", ctypes.c_longlong), ("head", ctypes.c_longlong),
+                ("seq", ctypes.c_longlong)]
+
+
+class FaLayout(ctypes.Structure):
+    """fa_layout: the strides of every operand of a call."""
+    _fields_ = [(n, FaStrides) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv")]
+
+
 class FattnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -73,6 +84,10 @@ def load(path: str | None = None):
             "fa_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
             "fa_selftest_wait_timeout": (i, [i, vp]),
             "fa_bwd_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]),
+            "fa_fwd_strided": (i, [vp, vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(FaLayout), f,
+                                   i, i, vp]),
+            "fa_bwd_strided": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
+                                   ctypes.POINTER(FaLayout), f, i, i, i, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -131,6 +146,48 @@ def _check_tensors(*ts):
             raise ValueError("libfattn takes CUDA tensors only")
         if not t.is_contiguous():
             raise ValueError("libfattn takes contiguous tensors only")
+
+
+def strides_of(t, dims: str = "bhnd") -> FaStrides:
+    """fa_strides of a 4-D tensor whose dimensions are named by `dims` (a
+    permutation of "bhnd"); D must be the contiguous dimension."""
+    if t.dim() != 4 or sorted(dims) != sorted("bhnd"):
+        raise ValueError(f"expected a 4-D tensor and a permutation of 'bhnd', got {dims!r}")
+    st = t.stride()
+    if st[dims.index("d")] != 1:
+        raise ValueError("the head dimension D must be contiguous")
+    return FaStrides(st[dims.index("b")], st[dims.index("h")], st[dims.index("n")])
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libfattn takes CUDA tensors only")
+
+
+def fa_fwd_strided(q, k, v, o, lse, layout: FaLayout, B: int, H: int, N: int, D: int,
+                   scale: float, causal: bool, stream=None):
+    """fa_fwd on operands in the layout `layout` (see fa_fwd_strided)."""
+    _check_cuda(q, k, v, o, lse)
+    st = load().fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                               ctypes.byref(layout), float(scale), int(bool(causal)),
+                               _dtype_code(q), _stream(stream))
+    _check(st, "fa_fwd_strided")
+
+
+def fa_bwd_strided(q, k, v, o, lse, do, dq, dk, dv, layout: FaLayout, B: int, H: int, N: int,
+                   D: int, scale: float, causal: bool, deterministic: bool = False,
+                   workspace=None, stream=None):
+    """fa_bwd on operands in the layout `layout` (see fa_bwd_strided)."""
+    _check_cuda(q, k, v, o, lse, do, dq, dk, dv, workspace)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, D, deterministic, q.device)
+    st = load().fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, D, ctypes.byref(layout),
+                               float(scale), int(bool(causal)), _dtype_code(q),
+                               int(bool(deterministic)), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check(st, "fa_bwd_strided")
 
 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):

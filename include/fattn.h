@@ -18,9 +18,11 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *   Layout   Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, D] arrays of
- *            16-bit floats, D innermost ([WALK] sec. 1.1, "Q, K, V: (batch,
- *            heads, seq_len, dim)").  LSE and Di are contiguous fp32 [B, H, N].
+ *   Layout   Q, K, V, O, dO, dQ, dK, dV are [B, H, N, D] arrays of 16-bit
+ *            floats, D innermost ([WALK] sec. 1.1, "Q, K, V: (batch, heads,
+ *            seq_len, dim)"): contiguous for the plain entry points, any
+ *            strides (fa_layout) for the *_strided ones.  LSE and Di are
+ *            contiguous fp32 [B, H, N].
  *            Q, K and V share N (self-attention).
  *   Types    FA_BF16 or FA_FP16, the same for every 16-bit array of a call.
  *            Accumulation and softmax statistics are fp32 ([WALK] sec. 5.2).
@@ -67,6 +69,28 @@ int fa_abi_version(void);
 const char* fa_status_string(fa_status s);
 
 /*
+ * Element strides of one [B, H, N, D] operand whose D elements are
+ * contiguous: element (b, h, n, d) lives at base + b*batch + h*head + n*seq + d
+ * (in elements, not bytes).  The contiguous layout is {H*N*D, N*D, D}; the
+ * [API] flash_attn_func layout (batch, seqlen, nheads, headdim) is
+ * {N*H*D, D, H*D}; a packed (batch, seqlen, 3, nheads, headdim) QKV tensor
+ * gives Q, K and V with {3*N*H*D, D, 3*H*D} at offsets 0, H*D and 2*H*D.
+ * Each stride must be a non-negative multiple of 8 (16 bytes, a TMA rule),
+ * and every element must lie less than 2^40 bytes from its base.
+ * Outputs must not overlap each other or themselves (not checked).
+ */
+typedef struct {
+  long long batch, head, seq;
+} fa_strides;
+
+/* The strides of every operand of a call.  fa_fwd_strided reads q, k, v and
+ * o; fa_bwd_strided reads all eight.  LSE, Di and the workspace keep their
+ * fixed contiguous layouts. */
+typedef struct {
+  fa_strides q, k, v, o, dO, dq, dk, dv;
+} fa_layout;
+
+/*
  * Forward pass ([WALK] sec. 2.4 and 3.1; [DEEP] online softmax).
  *
  *   o[b,h,i,:]  = sum_j P_ij V[b,h,j,:],  P = softmax_j(scale * Q_i . K_j)
@@ -79,6 +103,16 @@ const char* fa_status_string(fa_status s);
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int D, float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * fa_fwd on operands in any layout described by `layout` (see fa_strides);
+ * the arithmetic, and so the result, is bit-identical to fa_fwd on the same
+ * values stored contiguously.  layout == NULL or a bad stride returns
+ * FA_ERR_INVALID_ARG before anything is enqueued.
+ */
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int D, const fa_layout* layout, float scale, int causal,
+                         fa_dtype dtype, void* stream);
 
 /*
  * Workspace bytes fa_bwd needs, laid out as (each part 256-byte aligned):
@@ -111,6 +145,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
                  float scale, int causal, fa_dtype dtype, int deterministic, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd on operands in any layout described by `layout`; bit-identical to
+ * fa_bwd on the same values stored contiguously.  The workspace is the same
+ * size and layout as for fa_bwd.
+ */
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int D, const fa_layout* layout, float scale, int causal,
+                         fa_dtype dtype, int deterministic, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * The stages fa_bwd enqueues, for callers that schedule or time them

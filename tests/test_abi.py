@@ -11,8 +11,8 @@ from exact_attention_93_gb300 import build, fattn
 NULL = None
 EXPECTED = [
     "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert", "fa_bwd_noalloc",
-    "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_device_error", "fa_fwd",
-    "fa_selftest_wait_timeout", "fa_status_string",
+    "fa_bwd_preprocess", "fa_bwd_strided", "fa_bwd_workspace_size", "fa_device_error", "fa_fwd",
+    "fa_fwd_strided", "fa_selftest_wait_timeout", "fa_status_string",
 ]
 
 
@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 1
+    assert lib.fa_abi_version() == 2
     names = [lib.fa_status_string(i).decode() for i in range(5)]
     assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
                      "FA_ERR_TIMEOUT"]
@@ -117,3 +117,64 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fattn.fa_fwd(q, q, q, q, torch.zeros(1, 1, 128), 0.125, False)
+
+
+def contiguous(B, H, N, D):
+    return fattn.FaStrides(H * N * D, N * D, D)
+
+
+def layout_with(**bad):
+    c = contiguous(1, 2, 128, 64)
+    L = fattn.FaLayout(*([c] * 8))
+    for name, st in bad.items():
+        setattr(L, name, st)
+    return L
+
+
+def fwd_strided(lib, L, B=1, H=2, N=128, D=64):
+    return lib.fa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, N, D, ctypes.byref(L),
+                              ctypes.c_float(0.125), 0, 0, NULL)
+
+
+def bwd_strided(lib, L, B=1, H=2, N=128, D=64):
+    need = lib.fa_bwd_workspace_size(B, H, N, D, 0)
+    return lib.fa_bwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, N, D,
+                              ctypes.byref(L), ctypes.c_float(0.125), 0, 0, 0, FAKE, need, NULL)
+
+
+@pytest.mark.parametrize("bad", [
+    {"q": fattn.FaStrides(2 * 128 * 64, 128 * 64, 68)},    # seq stride not a multiple of 8
+    {"k": fattn.FaStrides(2 * 128 * 64, 4, 64)},            # head stride not a multiple of 8
+    {"v": fattn.FaStrides(-8, 128 * 64, 64)},               # negative
+    {"o": fattn.FaStrides(0, 1 << 39, 64)},                # head 1 lies 2^40 bytes from the base
+])
+def test_strided_entry_points_reject_bad_strides(lib, bad):
+    L = layout_with(**bad)
+    assert fwd_strided(lib, L) == fattn.FA_ERR_INVALID_ARG
+    assert bwd_strided(lib, L) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_strided_backward_checks_gradient_strides(lib):
+    L = layout_with(dk=fattn.FaStrides(2 * 128 * 64, 128 * 64, 12))
+    assert bwd_strided(lib, L) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_strided_entry_points_need_a_layout(lib):
+    assert lib.fa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, None,
+                              ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64,
+                              None, ctypes.c_float(0.125), 0, 0, 0, FAKE, 1 << 40,
+                              NULL) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_strides_of_reads_named_dimensions():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(2, 5, 3, 64)                      # (batch, seqlen, nheads, headdim)
+    s = fattn.strides_of(x, "bnhd")
+    assert (s.batch, s.head, s.seq) == (5 * 3 * 64, 64, 3 * 64)
+    qkv = torch.zeros(2, 5, 3, 4, 128)                # packed (batch, seqlen, 3, nheads, headdim)
+    k = qkv[:, :, 1]
+    s = fattn.strides_of(k, "bnhd")
+    assert (s.batch, s.head, s.seq) == (5 * 3 * 4 * 128, 128, 3 * 4 * 128)
+    with pytest.raises(ValueError):
+        fattn.strides_of(x.transpose(2, 3), "bnhd")   # D not contiguous
