@@ -56,6 +56,12 @@ def _bind(path: str):
         ctypes.c_int, lp, ctypes.c_long, dp, dp, dp, dp, ctypes.c_long,
         ctypes.c_long, dp, dp,
     ]
+    lib.fa_oracle_rows_ex.restype = ctypes.c_int
+    lib.fa_oracle_rows_ex.argtypes = [
+        dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.c_int, ctypes.c_long, ctypes.c_long, ctypes.c_double, lp, ctypes.c_long,
+        dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, dp, dp,
+    ]
     lib.fa_oracle_threads.restype = ctypes.c_int
     lib.fa_oracle_threads.argtypes = []
     lib.fa_oracle_set_threads.restype = None
@@ -100,12 +106,15 @@ def _ptr(a):
 
 
 def attention_head(q, k, v, scale, causal, dout=None, rows=None,
-                   kv_range=None, want_grads=True):
+                   kv_range=None, want_grads=True, window=(-1, -1), alibi_slope=0.0):
     """Exact attention for one (batch, head) slice.
 
     q, k, v, dout: [N, D].  rows: query-row indices (default: all rows).
     kv_range: (begin, end) key range for dK/dV column sums (default: all keys
     when every row is requested, none otherwise).
+    window: (left, right); query i sees keys i - left .. i + right, a
+    negative bound being absent.  alibi_slope: the score of (i, j) gets
+    -alibi_slope * |i - j| added after scaling.
 
     Returns a dict with o [R, D], lse [R] and, when dout is given, dq [R, D],
     di [R] and (if a key range applies) dk, dv [end - begin, D].
@@ -137,12 +146,14 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
             kb, ke = int(kv_range[0]), int(kv_range[1])
             dk = np.empty((ke - kb, D), np.float64)
             dv = np.empty((ke - kb, D), np.float64)
-    rc = lib.fa_oracle_rows(
+    left, right = (int(x) for x in window)
+    rc = lib.fa_oracle_rows_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, D, float(scale), int(bool(causal)),
+        left, right, float(alibi_slope),
         rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if rows_arr is not None else None,
         R, _ptr(o), _ptr(lse), _ptr(dq), _ptr(di), kb, ke, _ptr(dk), _ptr(dv))
     if rc != 0:
-        raise RuntimeError(f"fa_oracle_rows failed with code {rc}")
+        raise RuntimeError(f"fa_oracle_rows_ex failed with code {rc}")
     out = {"o": o, "lse": lse}
     if dq is not None:
         out["dq"] = dq
@@ -153,12 +164,18 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
     return out
 
 
-def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None):
+def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None,
+              window=(-1, -1), alibi_slopes=None):
     """Exact attention over a [B, H, N, D] batch, one (b, h) slice at a time.
 
     rows: None (every row) or a callable (b, h) -> row indices, or an array of
-    shape [B, H, R].  Returns arrays shaped [B, H, R, ...]."""
+    shape [B, H, R].  alibi_slopes: None, [H] or [B, H].  Returns arrays
+    shaped [B, H, R, ...]."""
     B, H, N, D = tuple(q.shape)
+    slopes = np.zeros((B, H))
+    if alibi_slopes is not None:
+        a = _f64(alibi_slopes)
+        slopes = np.broadcast_to(a, (B, H)) if a.ndim == 1 else a.reshape(B, H)
     res = {}
     for b in range(B):
         for h in range(H):
@@ -170,7 +187,7 @@ def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None):
                 r = rows[b][h]
             one = attention_head(q[b, h], k[b, h], v[b, h], scale, causal,
                                  None if dout is None else dout[b, h], r,
-                                 kv_range)
+                                 kv_range, window=window, alibi_slope=slopes[b, h])
             for key, val in one.items():
                 res.setdefault(key, []).append(val)
     for key in list(res):

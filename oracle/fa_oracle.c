@@ -12,6 +12,11 @@
  *            "FlashAttention 深入", section on the standard attention problem)
  *   S_ij  = -inf for j > i when causal                    query i sees keys j <= i
  *           (l189.com walkthrough, sec. 5.3, causal mask)
+ *   S_ij  = -inf unless i - left <= j <= i + right        sliding window, each
+ *           bound absent when negative (claire-chang.com FlashAttention
+ *           introduction, flash_attn_func window_size)
+ *   S_ij += -slope * |i - j|                              ALiBi bias on the
+ *           scaled score (same page, alibi_slopes)
  *   m_i   = max_j S_ij
  *   P_ij  = exp(S_ij - m_i) / sum_k exp(S_ik - m_i)       max-shifted softmax
  *           (l189.com walkthrough, sec. 2.2 and sec. 5.2)
@@ -59,23 +64,31 @@ void fa_oracle_set_threads(int n) {
 
 /* One query row: materialise the score row S_i. and probability row P_i.,
  * then O_i, LSE_i and (if dout != NULL) dP_i., Di, dS_i. and dQ_i. */
+/* Is key j visible to query i? */
+static int visible(long i, long j, int causal, long left, long right) {
+    if (causal && j > i) return 0;
+    if (left >= 0 && j < i - left) return 0;
+    if (right >= 0 && j > i + right) return 0;
+    return 1;
+}
+
 static void one_row(const double* q, const double* k, const double* v,
                     const double* dout, long N, long D, double scale,
-                    int causal, long i, double* s_row, double* p_row,
-                    double* ds_row, double* o_i, double* lse_i, double* dq_i,
-                    double* di_i) {
+                    int causal, long left, long right, double slope, long i,
+                    double* s_row, double* p_row, double* ds_row, double* o_i,
+                    double* lse_i, double* dq_i, double* di_i) {
     const double* qi = q + i * D;
 
-    /* scores S_ij = scale * Q_i . K_j, masked to -inf above the diagonal */
+    /* scores S_ij = scale * Q_i . K_j - slope * |i - j|, -inf where masked */
     for (long j = 0; j < N; ++j) {
-        if (causal && j > i) {
+        if (!visible(i, j, causal, left, right)) {
             s_row[j] = -INFINITY;
             continue;
         }
         const double* kj = k + j * D;
         double acc = 0.0;
         for (long d = 0; d < D; ++d) acc += qi[d] * kj[d];
-        s_row[j] = scale * acc;
+        s_row[j] = scale * acc - slope * (double)labs(i - j);
     }
 
     /* row maximum over visible keys */
@@ -83,15 +96,17 @@ static void one_row(const double* q, const double* k, const double* v,
     for (long j = 0; j < N; ++j)
         if (s_row[j] > m) m = s_row[j];
 
-    /* softmax with the maximum subtracted */
+    /* softmax with the maximum subtracted; a row that sees no key has
+     * O = 0 and LSE = -inf */
     double denom = 0.0;
     for (long j = 0; j < N; ++j) {
         double e = (s_row[j] == -INFINITY) ? 0.0 : exp(s_row[j] - m);
         p_row[j] = e;
         denom += e;
     }
-    for (long j = 0; j < N; ++j) p_row[j] /= denom;
-    *lse_i = m + log(denom);
+    if (denom > 0.0)
+        for (long j = 0; j < N; ++j) p_row[j] /= denom;
+    *lse_i = denom > 0.0 ? m + log(denom) : -INFINITY;
 
     /* O_i = sum_j P_ij V_j */
     for (long d = 0; d < D; ++d) o_i[d] = 0.0;
@@ -134,8 +149,20 @@ int fa_oracle_rows(const double* q, const double* k, const double* v,
                    int causal, const long* rows, long nrows, double* o,
                    double* lse, double* dq, double* di, long kv_begin,
                    long kv_end, double* dk, double* dv) {
+    return fa_oracle_rows_ex(q, k, v, dout, N, D, scale, causal, -1, -1, 0.0,
+                             rows, nrows, o, lse, dq, di, kv_begin, kv_end, dk,
+                             dv);
+}
+
+int fa_oracle_rows_ex(const double* q, const double* k, const double* v,
+                      const double* dout, long N, long D, double scale,
+                      int causal, long left, long right, double slope,
+                      const long* rows, long nrows, double* o, double* lse,
+                      double* dq, double* di, long kv_begin, long kv_end,
+                      double* dk, double* dv) {
     if (!q || !k || !v || !o || !lse || N < 1 || D < 1 || nrows < 0)
         return 1;
+    if (left < -1 || right < -1 || !isfinite(slope)) return 1;
     if ((dq || di || dk || dv) && !dout) return 1;
     int want_cols = (dk != NULL) || (dv != NULL);
     if (want_cols && (kv_begin < 0 || kv_end > N || kv_begin > kv_end))
@@ -166,7 +193,8 @@ int fa_oracle_rows(const double* q, const double* k, const double* v,
 #pragma omp parallel for schedule(dynamic, 1)
     for (long r = 0; r < nrows; ++r) {
         long i = rows ? rows[r] : r;
-        one_row(q, k, v, dout, N, D, scale, causal, i, s_all + (size_t)r * N,
+        one_row(q, k, v, dout, N, D, scale, causal, left, right, slope, i,
+                s_all + (size_t)r * N,
                 p_all + (size_t)r * N, dout ? ds_all + (size_t)r * N : NULL,
                 o + (size_t)r * D, lse + r, dq ? dq + (size_t)r * D : NULL,
                 di_tmp + r);

@@ -31,6 +31,19 @@ int fa_oracle_rows(const double* q, const double* k, const double* v,
                    double* lse, double* dq, double* di, long kv_begin,
                    long kv_end, double* dk, double* dv);
 
+/*
+ * fa_oracle_rows with a sliding window and an ALiBi bias: query i sees key j
+ * only when i - left <= j <= i + right (a bound of -1 is absent; with causal
+ * also j <= i), and the scaled score gets -slope * |i - j| added.
+ * fa_oracle_rows is this with left = right = -1 and slope = 0.
+ */
+int fa_oracle_rows_ex(const double* q, const double* k, const double* v,
+                      const double* dout, long N, long D, double scale,
+                      int causal, long left, long right, double slope,
+                      const long* rows, long nrows, double* o, double* lse,
+                      double* dq, double* di, long kv_begin, long kv_end,
+                      double* dk, double* dv);
+
 /* OpenMP threads the next call will use, and a way to set them. */
 int fa_oracle_threads(void);
 void fa_oracle_set_threads(int n);

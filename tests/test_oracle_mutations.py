@@ -16,11 +16,11 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.c")
 # (name, original text, planted mistake)
 MUTANTS = [
     ("causal mask includes no diagonal", "if (causal && j > i)", "if (causal && j >= i)"),
-    ("causal mask off", "if (causal && j > i)", "if (causal && j > i + N)"),
-    ("scale dropped from scores", "s_row[j] = scale * acc;", "s_row[j] = acc;"),
+    ("causal mask off", "if (causal && j > i)", "if (causal && j > i + 1000000000L)"),
+    ("scale dropped from scores", "s_row[j] = scale * acc", "s_row[j] = acc"),
     ("no max shift", "if (s_row[j] > m) m = s_row[j];", "if (s_row[j] > m) m = 0.0;"),
     ("softmax not normalised", "for (long j = 0; j < N; ++j) p_row[j] /= denom;", ";"),
-    ("lse misses the max", "*lse_i = m + log(denom);", "*lse_i = log(denom);"),
+    ("lse misses the max", "? m + log(denom)", "? log(denom)"),
     ("output uses keys instead of values", "const double* vj = v + j * D;\n        for (long d = 0; d < D; ++d) o_i[d]",
      "const double* vj = k + j * D;\n        for (long d = 0; d < D; ++d) o_i[d]"),
     ("dP uses keys", "for (long d = 0; d < D; ++d) acc += doi[d] * vj[d];",
@@ -35,6 +35,14 @@ MUTANTS = [
     ("dK misses scale", "for (long d = 0; d < D; ++d) dkj[d] *= scale;", ";"),
     ("dV uses dS", "double p = p_all[(size_t)r * N + j];", "double p = ds_all[(size_t)r * N + j];"),
     ("dK uses dO", "const double* qi = q + i * D;\n                    for", "const double* qi = dout + i * D;\n                    for"),
+    ("window left bound off by one", "j < i - left", "j <= i - left"),
+    ("window left bound ignored", "if (left >= 0 && j < i - left) return 0;", ";"),
+    ("window right bound ignored", "if (right >= 0 && j > i + right) return 0;", ";"),
+    ("window bounds swapped", "j > i + right", "j > i + left"),
+    ("alibi sign flipped", "- slope * (double)labs(i - j)", "+ slope * (double)labs(i - j)"),
+    ("alibi without absolute value", "(double)labs(i - j)", "(double)(i - j)"),
+    ("alibi scaled with the scores", "s_row[j] = scale * acc - slope * (double)labs(i - j);",
+     "s_row[j] = scale * (acc - slope * (double)labs(i - j));"),
 ]
 
 
@@ -51,6 +59,11 @@ def run_pins():
         ("sdpa_nc", lambda: pins.test_matches_torch_sdpa_float64_forward_and_gradients(19, 8, False)),
         ("finite_diff", lambda: pins.test_gradients_by_central_differences(4, 3, True)),
         ("invariants", lambda: pins.test_gradient_invariants_and_di_identity(True)),
+        ("band_bf", lambda: pins.test_window_and_alibi_brute_force(2, 1, 0.0, False)),
+        ("band_bf_c", lambda: pins.test_window_and_alibi_brute_force(3, -1, 0.0, True)),
+        ("alibi_bf", lambda: pins.test_window_and_alibi_brute_force(2, 3, 0.25, False)),
+        ("band_sdpa", lambda: pins.test_window_and_alibi_match_torch_sdpa_float64(5, 3, 0.0, False)),
+        ("alibi_closed", pins.test_alibi_at_zero_scale_is_a_closed_form),
     ]
     for name, fn in checks:
         try:

@@ -414,3 +414,160 @@ def test_large_scores_concentrate_on_the_argmax_without_overflow():
     # causal row 1 sees keys 0 and 1 only: the argmax there is key 1
     np.testing.assert_allclose(rc["o"][1], v[1], rtol=0, atol=1e-15)
     assert rc["lse"][1] == pytest.approx(900.0, abs=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Sliding window and ALiBi (claire-chang.com FlashAttention introduction,
+# flash_attn_func: window_size = (left, right), query i sees keys
+# i - left .. i + right inclusive, -1 meaning no bound; alibi_slopes adds
+# -slope * |i - j| to the score of query i and key j)
+# --------------------------------------------------------------------------
+
+def brute_force_banded(q, k, v, scale, causal, left, right, slope):
+    """The definition with math.exp, written apart from the oracle."""
+    n, d = q.shape
+    o = np.zeros((n, d))
+    lse = np.zeros(n)
+    for i in range(n):
+        s = []
+        for j in range(n):
+            if causal and j > i:
+                continue
+            if left != -1 and j < i - left:
+                continue
+            if right != -1 and j > i + right:
+                continue
+            s.append((j, scale * sum(q[i, t] * k[j, t] for t in range(d)) - slope * abs(i - j)))
+        z = sum(math.exp(val) for _, val in s)
+        lse[i] = math.log(z)
+        for j, val in s:
+            for t in range(d):
+                o[i, t] += math.exp(val) / z * v[j, t]
+    return o, lse
+
+
+BANDS = [(-1, -1, 0.0), (2, 1, 0.0), (0, 0, 0.0), (3, -1, 0.0), (-1, 2, 0.0),
+         (-1, -1, 0.5), (2, 3, 0.25), (1, -1, 1.5)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("left,right,slope", BANDS)
+def test_window_and_alibi_brute_force(left, right, slope, causal):
+    n, d = 7, 3
+    q, k, v = rnd((n, d), 70), rnd((n, d), 71), rnd((n, d), 72)
+    o_bf, lse_bf = brute_force_banded(q, k, v, 0.8, causal, left, right, slope)
+    r = oracle.attention_head(q, k, v, 0.8, causal, window=(left, right), alibi_slope=slope)
+    np.testing.assert_allclose(r["o"], o_bf, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(r["lse"], lse_bf, rtol=0, atol=1e-13)
+
+
+def additive_mask(n, causal, left, right, slope):
+    """[n, n] float64 mask for torch SDPA: the ALiBi bias where visible,
+    -inf elsewhere."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    ok = np.ones((n, n), bool)
+    if causal:
+        ok &= j <= i
+    if left != -1:
+        ok &= j >= i - left
+    if right != -1:
+        ok &= j <= i + right
+    return np.where(ok, -slope * np.abs(i - j), -np.inf)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("left,right,slope", [(5, 3, 0.0), (-1, -1, 0.3), (4, 0, 0.7),
+                                              (0, 6, 0.1)])
+def test_window_and_alibi_match_torch_sdpa_float64(left, right, slope, causal):
+    n, d = 23, 8
+    q, k, v, do = (rnd((n, d), s) for s in (80, 81, 82, 83))
+    scale = 1.0 / math.sqrt(d)
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    mask = torch.tensor(additive_mask(n, causal, left, right, slope))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], attn_mask=mask[None, None],
+        scale=scale)[0, 0]
+    out.backward(torch.tensor(do))
+    r = oracle.attention_head(q, k, v, scale, causal, dout=do, window=(left, right),
+                              alibi_slope=slope)
+    np.testing.assert_allclose(r["o"], out.detach().numpy(), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(r["dq"], tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dk"], tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dv"], tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_zero_is_the_identity_map():
+    """window (0, 0): each query sees only its own key, so O = V and
+    LSE_i = scale * Q_i . K_i."""
+    n, d = 9, 4
+    q, k, v = rnd((n, d), 90), rnd((n, d), 91), rnd((n, d), 92)
+    r = oracle.attention_head(q, k, v, 0.6, False, window=(0, 0))
+    np.testing.assert_allclose(r["o"], v, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(r["lse"], 0.6 * (q * k).sum(1), rtol=0, atol=1e-13)
+
+
+def test_causal_equals_window_with_no_right_reach():
+    n, d = 12, 4
+    q, k, v, do = (rnd((n, d), s) for s in (93, 94, 95, 96))
+    a = oracle.attention_head(q, k, v, 0.5, True, dout=do)
+    b = oracle.attention_head(q, k, v, 0.5, False, dout=do, window=(-1, 0))
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(a[key], b[key], rtol=0, atol=1e-14)
+
+
+def test_alibi_at_zero_scale_is_a_closed_form():
+    """scale = 0 leaves only the bias: P_ij is proportional to exp(-slope |i-j|)
+    and LSE_i = ln sum_j exp(-slope |i - j|)."""
+    n, d, slope = 6, 3, 0.9
+    q, k, v = rnd((n, d), 97), rnd((n, d), 98), rnd((n, d), 99)
+    r = oracle.attention_head(q, k, v, 0.0, False, alibi_slope=slope)
+    for i in range(n):
+        w = np.array([math.exp(-slope * abs(i - j)) for j in range(n)])
+        np.testing.assert_allclose(r["lse"][i], math.log(w.sum()), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(r["o"][i], (w / w.sum()) @ v, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_and_alibi_gradients_by_central_differences(causal):
+    n, d = 6, 3
+    q, k, v, do = rnd((n, d), 100), rnd((n, d), 101), rnd((n, d), 102), rnd((n, d), 103)
+    scale, h, win, slope = 0.7, 1e-6, (2, 1), 0.4
+    r = oracle.attention_head(q, k, v, scale, causal, dout=do, window=win, alibi_slope=slope)
+
+    def loss(q, k, v):
+        o = oracle.attention_head(q, k, v, scale, causal, window=win, alibi_slope=slope)["o"]
+        return float((o * do).sum())
+
+    for name, arr, grad in (("q", q, r["dq"]), ("k", k, r["dk"]), ("v", v, r["dv"])):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name] = arr.copy()
+            args_m[name] = arr.copy()
+            args_p[name][idx] += h
+            args_m[name][idx] -= h
+            fd[idx] = (loss(**args_p) - loss(**args_m)) / (2 * h)
+        err = np.abs(fd - grad).max() / max(np.abs(grad).max(), 1e-3)
+        assert err <= 1e-6, (name, err)
+
+
+def test_batched_alibi_slopes_are_per_head_or_per_batch_and_head():
+    B, H, n, d = 2, 3, 5, 2
+    x = [rnd((B, H, n, d), s) for s in (104, 105, 106)]
+    per_head = np.array([0.1, 0.5, 1.0])
+    a = oracle.attention(*x, 0.5, False, alibi_slopes=per_head)
+    b = oracle.attention(*x, 0.5, False, alibi_slopes=np.tile(per_head, (B, 1)))
+    np.testing.assert_array_equal(a["o"], b["o"])
+    for bb in range(B):
+        for hh in range(H):
+            one = oracle.attention_head(x[0][bb, hh], x[1][bb, hh], x[2][bb, hh], 0.5, False,
+                                        alibi_slope=per_head[hh])
+            np.testing.assert_array_equal(a["o"][bb, hh], one["o"])
+
+
+def test_window_bounds_below_minus_one_are_rejected():
+    q = rnd((4, 2), 107)
+    with pytest.raises(RuntimeError):
+        oracle.attention_head(q, q, q, 0.5, False, window=(-2, 0))
