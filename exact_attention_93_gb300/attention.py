@@ -6,8 +6,11 @@ claire-chang.com introduction ([API]): q, k, v of shape
 causal, deterministic; and the packed variant taking one
 (batch, seqlen, 3, nheads, headdim) tensor.  Both run the library's kernels
 on the caller's tensors in place through the strided C ABI (fa_fwd_strided,
-fa_bwd_strided): no transposes or copies of Q, K, V.  Dropout, sliding
-windows and ALiBi are not provided; asking for them raises.
+fa_bwd_ex): no transposes or copies of Q, K, V.  window_size gives
+sliding-window local attention (query i sees keys i - left .. i + right,
+-1 meaning no bound) and alibi_slopes ([nheads] or [batch, nheads] fp32) adds
+-slope * |i - j| to each score, as the page documents.  Dropout is not
+provided; asking for it raises.
 """
 from __future__ import annotations
 
@@ -18,13 +21,17 @@ from . import fattn
 __all__ = ["flash_attn_func", "flash_attn_qkvpacked_func"]
 
 
-def _check_options(dropout_p, window_size, alibi_slopes):
+def _check_options(dropout_p, window_size, alibi_slopes, B, H):
     if dropout_p:
         raise NotImplementedError("dropout is not supported (dropout_p must be 0)")
-    if tuple(window_size) != (-1, -1):
-        raise NotImplementedError("sliding-window attention is not supported yet")
+    left, right = (int(x) for x in window_size)
+    if left < -1 or right < -1:
+        raise ValueError("window_size bounds must be >= -1 (-1: no bound)")
     if alibi_slopes is not None:
-        raise NotImplementedError("ALiBi is not supported yet")
+        if tuple(alibi_slopes.shape) not in ((H,), (B, H)):
+            raise ValueError("alibi_slopes must have shape (nheads,) or (batch, nheads)")
+        alibi_slopes = alibi_slopes.to(torch.float32).contiguous()
+    return (left, right), alibi_slopes
 
 
 def _bnhd(t) -> fattn.FaStrides:
@@ -46,28 +53,30 @@ def _layout(q, k, v, o, do=None, dq=None, dk=None, dv=None) -> fattn.FaLayout:
                           _bnhd(dk) if dk is not None else z, _bnhd(dv) if dv is not None else z)
 
 
-def _forward(q, k, v, scale, causal):
+def _forward(q, k, v, scale, causal, window, slopes):
     B, N, H, D = (int(x) for x in q.shape)
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k and v must have the same (batch, seqlen, nheads, headdim) shape")
     o = torch.empty((B, N, H, D), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fattn.fa_fwd_strided(q, k, v, o, lse, _layout(q, k, v, o), B, H, N, D, scale, causal)
+    fattn.fa_fwd_ex(q, k, v, o, lse, _layout(q, k, v, o), fattn.options(window, slopes),
+                    B, H, N, D, scale, causal)
     return o, lse
 
 
-def _backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, deterministic):
+def _backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, window, slopes, deterministic):
     B, N, H, D = (int(x) for x in q.shape)
-    fattn.fa_bwd_strided(q, k, v, o, lse, do, dq, dk, dv, _layout(q, k, v, o, do, dq, dk, dv),
-                         B, H, N, D, scale, causal, deterministic)
+    fattn.fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, _layout(q, k, v, o, do, dq, dk, dv),
+                    fattn.options(window, slopes), B, H, N, D, scale, causal, deterministic)
 
 
 class _FlashAttn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal, deterministic):
-        o, lse = _forward(q, k, v, scale, causal)
+    def forward(ctx, q, k, v, scale, causal, window, slopes, deterministic):
+        o, lse = _forward(q, k, v, scale, causal, window, slopes)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.scale, ctx.causal, ctx.deterministic = scale, causal, deterministic
+        ctx.slopes = slopes
+        ctx.scale, ctx.causal, ctx.window, ctx.deterministic = scale, causal, window, deterministic
         ctx.mark_non_differentiable(lse)
         return o, lse
 
@@ -76,17 +85,18 @@ class _FlashAttn(torch.autograd.Function):
         q, k, v, o, lse = ctx.saved_tensors
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
-                  ctx.deterministic)
-        return dq, dk, dv, None, None, None
+                  ctx.window, ctx.slopes, ctx.deterministic)
+        return dq, dk, dv, None, None, None, None, None
 
 
 class _FlashAttnQKVPacked(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, qkv, scale, causal, deterministic):
+    def forward(ctx, qkv, scale, causal, window, slopes, deterministic):
         q, k, v = qkv.unbind(dim=2)
-        o, lse = _forward(q, k, v, scale, causal)
+        o, lse = _forward(q, k, v, scale, causal, window, slopes)
         ctx.save_for_backward(qkv, o, lse)
-        ctx.scale, ctx.causal, ctx.deterministic = scale, causal, deterministic
+        ctx.slopes = slopes
+        ctx.scale, ctx.causal, ctx.window, ctx.deterministic = scale, causal, window, deterministic
         ctx.mark_non_differentiable(lse)
         return o, lse
 
@@ -97,8 +107,8 @@ class _FlashAttnQKVPacked(torch.autograd.Function):
         dqkv = torch.empty_like(qkv)
         dq, dk, dv = dqkv.unbind(dim=2)
         _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
-                  ctx.deterministic)
-        return dqkv, None, None, None
+                  ctx.window, ctx.slopes, ctx.deterministic)
+        return dqkv, None, None, None, None, None
 
 
 def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=False,
@@ -107,11 +117,13 @@ def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=False,
     """Exact attention of q, k, v shaped (batch, seqlen, nheads, headdim),
     bf16 or fp16 CUDA tensors with headdim 64 or 128 contiguous.  Returns the
     output in the same shape (and the fp32 (batch, nheads, seqlen) log-sum-exp
-    of the scaled scores when return_lse).  Differentiable in q, k, v;
-    deterministic selects the two-pass dQ backward."""
-    _check_options(dropout_p, window_size, alibi_slopes)
+    of the scaled, biased scores when return_lse).  window_size = (left,
+    right) limits query i to keys i - left .. i + right (-1: no bound);
+    alibi_slopes adds -slope * |i - j|.  Differentiable in q, k, v (not in the
+    slopes); deterministic selects the two-pass dQ backward."""
+    window, slopes = _check_options(dropout_p, window_size, alibi_slopes, q.shape[0], q.shape[2])
     scale = q.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
-    o, lse = _FlashAttn.apply(q, k, v, scale, bool(causal), bool(deterministic))
+    o, lse = _FlashAttn.apply(q, k, v, scale, bool(causal), window, slopes, bool(deterministic))
     return (o, lse) if return_lse else o
 
 
@@ -120,9 +132,11 @@ def flash_attn_qkvpacked_func(qkv, dropout_p=0.0, softmax_scale=None, causal=Fal
                               return_lse=False):
     """flash_attn_func on one packed (batch, seqlen, 3, nheads, headdim)
     tensor; its gradient comes back in the same packed layout."""
-    _check_options(dropout_p, window_size, alibi_slopes)
     if qkv.dim() != 5 or qkv.shape[2] != 3:
         raise ValueError("expected qkv of shape (batch, seqlen, 3, nheads, headdim)")
+    window, slopes = _check_options(dropout_p, window_size, alibi_slopes, qkv.shape[0],
+                                    qkv.shape[3])
     scale = qkv.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
-    o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), bool(deterministic))
+    o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), window, slopes,
+                                       bool(deterministic))
     return (o, lse) if return_lse else o

@@ -99,6 +99,23 @@ fa_status check_strides(const Shape& s, const RowStrides& r) {
   return last * 2.0 < 1099511627776.0 ? FA_OK : FA_ERR_INVALID_ARG;
 }
 
+// The band of visible keys: the window of `opt` (absent when opt is null)
+// intersected with the causal mask (right bound 0), and the ALiBi slopes.
+fa_status make_band(const fa_options* opt, int causal, int H, Band* b) {
+  *b = Band{-1, -1, nullptr, 0};
+  if (opt) {
+    if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
+    if (opt->alibi_slopes && (reinterpret_cast<uintptr_t>(opt->alibi_slopes) & 3u) != 0)
+      return FA_ERR_INVALID_ARG;
+    b->win_left = opt->window_left;
+    b->win_right = opt->window_right;
+    b->alibi = opt->alibi_slopes;
+    b->alibi_bstride = opt->alibi_per_batch ? H : 0;
+  }
+  if (causal) b->win_right = 0;  // j <= i, and j <= i + right for any right >= 0
+  return FA_OK;
+}
+
 bool tile_map(CUtensorMap* m, const void* base, const Shape& s, int dtype, const RowStrides& r,
               int box_rows = kTile) {
   return operand_map(m, base, dtype == FA_BF16, s.B, s.H, s.N, s.D, r.batch, r.head, r.seq,
@@ -112,8 +129,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Everything the dK/dV and dQ kernels share.
 fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void* v,
                           const void* dO, void* dq, void* dk, void* dv, const Shape& s,
-                          const Layout& L, float scale, int causal, int dtype, int deterministic,
-                          void* ws) {
+                          const Layout& L, float scale, const Band& band, int dtype,
+                          int deterministic, void* ws) {
   *a = BwdLaunch{};
   if (!tile_map(&a->map_q, q, s, dtype, L.q) || !tile_map(&a->map_k, k, s, dtype, L.k) ||
       !tile_map(&a->map_v, v, s, dtype, L.v) || !tile_map(&a->map_do, dO, s, dtype, L.dO) ||
@@ -134,7 +151,7 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
   a->H = s.H;
   a->scale = scale;
   a->scale_log2 = scale * kLog2e;
-  a->causal = causal ? 1 : 0;
+  a->band = band;
   a->bf16 = dtype == FA_BF16 ? 1 : 0;
   a->err = error_word_ptr();
   return a->err ? FA_OK : FA_ERR_CUDA;
@@ -151,7 +168,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 2; }
+int fa_abi_version(void) { return 3; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -169,10 +186,12 @@ const char* fa_status_string(fa_status s) {
 namespace {
 
 fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
-                   const Shape& s, const Layout& L, float scale, int causal, int dtype,
-                   void* stream) {
+                   const Shape& s, const Layout& L, float scale, int causal,
+                   const fa_options* opt, int dtype, void* stream) {
   fa_status st = check_shape(s, dtype);
   if (st != FA_OK) return st;
+  Band band;
+  if ((st = make_band(opt, causal, s.H, &band)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
@@ -188,7 +207,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   a.D = s.D;
   a.H = s.H;
   a.scale_log2 = scale * kLog2e;
-  a.causal = causal ? 1 : 0;
+  a.band = band;
   a.bf16 = dtype == FA_BF16 ? 1 : 0;
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
@@ -197,10 +216,12 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
 
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dO, void* dq, void* dk, void* dv, const Shape& s, const Layout& L,
-                   float scale, int causal, int dtype, int deterministic, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+                   float scale, int causal, const fa_options* opt, int dtype, int deterministic,
+                   void* workspace, size_t workspace_bytes, void* stream) {
   fa_status st = check_shape(s, dtype);
   if (st != FA_OK) return st;
+  Band band;
+  if ((st = make_band(opt, causal, s.H, &band)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -210,7 +231,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
   // Build every descriptor before enqueueing anything.
   BwdLaunch a;
-  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, dk, dv, s, L, scale, causal, dtype,
+  if ((st = make_bwd_launch(&a, q, k, v, dO, dq, dk, dv, s, L, scale, band, dtype,
                             deterministic, workspace)) != FA_OK)
     return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -234,15 +255,24 @@ extern "C" {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int D, float scale, int causal, fa_dtype dtype, void* stream) {
   const Shape s{B, H, N, D};
-  return fwd_impl(q, k, v, o, lse, s, contiguous_layout(s), scale, causal, dtype, stream);
+  return fwd_impl(q, k, v, o, lse, s, contiguous_layout(s), scale, causal, nullptr, dtype,
+                  stream);
 }
 
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int D, const fa_layout* layout, float scale, int causal,
                          fa_dtype dtype, void* stream) {
   if (!layout) return FA_ERR_INVALID_ARG;
-  return fwd_impl(q, k, v, o, lse, Shape{B, H, N, D}, from_abi(*layout), scale, causal, dtype,
-                  stream);
+  return fwd_impl(q, k, v, o, lse, Shape{B, H, N, D}, from_abi(*layout), scale, causal, nullptr,
+                  dtype, stream);
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int D, const fa_layout* layout, const fa_options* options,
+                    float scale, int causal, fa_dtype dtype, void* stream) {
+  const Shape s{B, H, N, D};
+  return fwd_impl(q, k, v, o, lse, s, layout ? from_abi(*layout) : contiguous_layout(s), scale,
+                  causal, options, dtype, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic) {
@@ -282,8 +312,10 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
     return FA_ERR_INVALID_ARG;
   if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
+  Band band;
+  if ((st = make_band(nullptr, causal, H, &band)) != FA_OK) return st;
   if ((st = make_bwd_launch(&a, q, k, v, dO, nullptr, dk, dv, s, contiguous_layout(s), scale,
-                            causal, dtype, deterministic, workspace)) != FA_OK)
+                            band, dtype, deterministic, workspace)) != FA_OK)
     return st;
   return from_cuda(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
 }
@@ -299,8 +331,10 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     return FA_ERR_INVALID_ARG;
   if ((st = check_ws(s, 1, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
+  Band band;
+  if ((st = make_band(nullptr, causal, H, &band)) != FA_OK) return st;
   if ((st = make_bwd_launch(&a, q, k, v, dO, dq, nullptr, nullptr, s, contiguous_layout(s),
-                            scale, causal, dtype, 1, workspace)) != FA_OK)
+                            scale, band, dtype, 1, workspace)) != FA_OK)
     return st;
   return from_cuda(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
 }
@@ -324,8 +358,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, fa_dtype dtype, int deterministic, void* workspace,
                  size_t workspace_bytes, void* stream) {
   const Shape s{B, H, N, D};
-  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, s, contiguous_layout(s), scale, causal, dtype,
-                  deterministic, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, s, contiguous_layout(s), scale, causal,
+                  nullptr, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
@@ -335,7 +369,18 @@ fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void
                          size_t workspace_bytes, void* stream) {
   if (!layout) return FA_ERR_INVALID_ARG;
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, Shape{B, H, N, D}, from_abi(*layout), scale,
-                  causal, dtype, deterministic, workspace, workspace_bytes, stream);
+                  causal, nullptr, dtype, deterministic, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                    const fa_layout* layout, const fa_options* options, float scale, int causal,
+                    fa_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  const Shape s{B, H, N, D};
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, s,
+                  layout ? from_abi(*layout) : contiguous_layout(s), scale, causal, options, dtype,
+                  deterministic, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_device_error(void* stream, int* code) {

@@ -23,6 +23,7 @@
 // issuer.  Every wait is bounded.
 #include <climits>
 
+#include "fa_band.cuh"
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 
@@ -138,7 +139,7 @@ struct DkdvSmem {
   int abort_flag;
 };
 
-template <int D, bool kBf16, bool kCausal, bool kAtomicDq>
+template <int D, bool kBf16, bool kAlibi, bool kAtomicDq>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdLaunch p) {
   using Smem = DkdvSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -152,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int kt = static_cast<int>(blockIdx.x % n_tiles);
   const int k0 = kt * kTile;
-  const int it_begin = kCausal ? kt : 0;
-  const int n_it = n_tiles - it_begin;
+  const int wl = p.band.win_left, wr = p.band.win_right;
+  int it_begin, it_last;  // query tiles whose band reaches this key tile
+  band_query_tiles(k0, kTile, kTile, n_tiles, wl, wr, it_begin, it_last);
+  const int n_it = it_last - it_begin + 1;
 
   if (tid == 0) {
     mbar_init(&s.kv_full, 1);
@@ -271,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     const int r = tid;  // key row within the tile (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int q0 = (it_begin + it) * kTile;
@@ -285,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         break;
       }
       tc_fence_after();
-      const bool diag = kCausal && (q0 == k0);
+      const bool cut = band_cuts(q0, kTile, k0, kTile, wl, wr);
+      const int key = k0 + r;
 #pragma unroll 1
       for (int c = 0; c < kTile / 32; ++c) {
         uint32_t sr[32], dr[32];
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tmem_ld32(tdP + lane_off + c * 32, dr);
         tmem_ld_wait();
         uint32_t pk[16], dk[16];
+        const bool plain = !cut && !kAlibi;
 #pragma unroll
         for (int t = 0; t < 32; t += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[c * 32 + t]);
@@ -303,8 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int col = c * 32 + t + e;  // query index within the tile
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
-            if (diag && col < r) pe = 0.f;
+            float z = fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]);
+            float pe;
+            if (plain) {
+              pe = ex2_approx(z);
+            } else {
+              if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - q0 - col)), z);
+              pe = ex2_approx(z);
+              if (cut && !band_visible(q0 + col, key, wl, wr)) pe = 0.f;
+            }
             pv[e] = pe;
             dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
           }
@@ -433,7 +446,7 @@ struct Dkdv128Smem {
   int abort_flag;
 };
 
-template <bool kBf16, bool kCausal, bool kAtomicDq>
+template <bool kBf16, bool kAlibi, bool kAtomicDq>
 __global__ void __launch_bounds__(kD128Threads, 1)
     bwd_dkdv_d128_kernel(const __grid_constant__ BwdLaunch p) {
   constexpr int D = 128;
@@ -451,8 +464,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int kt = static_cast<int>(blockIdx.x % n_kt);
   const int k0 = kt * kTile;
-  const int it_begin = kCausal ? 2 * kt : 0;  // first 64-row query tile that sees a key here
-  const int n_it = n_q64 - it_begin;
+  const int wl = p.band.win_left, wr = p.band.win_right;
+  int it_begin, it_last;  // 64-row query tiles whose band reaches this key tile
+  band_query_tiles(k0, kTile, kQ64, n_q64, wl, wr, it_begin, it_last);
+  const int n_it = it_last - it_begin + 1;
 
   if (tid == 0) {
     mbar_init(&s.kv_full, 1);
@@ -650,6 +665,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     const int r = quad * 32 + lane;                // key row (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1, st = it % 3;
@@ -666,9 +682,9 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
       tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
       tmem_ld_wait();
-      const bool diag = kCausal && (q0 < k0 + kTile);
+      const bool cut = band_cuts(q0, kQ64, k0, kTile, wl, wr);
       uint32_t pk[16], dk[16];
-      if (!diag) {
+      if (!cut && !kAlibi) {
         // P = 2^(S * scale * log2 e - LSE2) and dS = P (dP - Di), two
         // columns per packed instruction: the elementwise warps share
         // their SM sub-partitions with the MMA-issuing warps, so every
@@ -695,7 +711,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           }
         }
       } else {
-        // diagonal tile: key k0 + r sees query q only when q >= k0 + r
+        // a tile the band cuts, or an ALiBi bias: key k0 + r, query q
         const int key = k0 + r;
 #pragma unroll
         for (int t = 0; t < 32; t += 4) {
@@ -706,8 +722,11 @@ __global__ void __launch_bounds__(kD128Threads, 1)
           float pv[4], dsv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]));
-            if (key > q0 + half * 32 + t + e) pe = 0.f;
+            const int q = q0 + half * 32 + t + e;
+            float z = fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]);
+            if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - q)), z);
+            float pe = ex2_approx(z);
+            if (cut && !band_visible(q, key, wl, wr)) pe = 0.f;
             pv[e] = pe;
             dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
           }
@@ -800,7 +819,7 @@ struct DqSmem {
   int abort_flag;
 };
 
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kAlibi>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdLaunch p) {
   using Smem = DqSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -809,13 +828,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kTile - 1) / kTile;
   const int Npad = n_tiles * kTile;
-  // Head-major; under the causal mask the longest query tiles go first.
+  // Head-major; when keys are bounded on the right only (causal) later
+  // query tiles see more keys and go first.
   const int bh = static_cast<int>(blockIdx.x / n_tiles);
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
-  const int qt = kCausal ? n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles)
-                         : static_cast<int>(blockIdx.x % n_tiles);
+  const int wl = p.band.win_left, wr = p.band.win_right;
+  const int qt = (wl < 0 && wr >= 0) ? n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles)
+                                     : static_cast<int>(blockIdx.x % n_tiles);
   const int q0 = qt * kTile;
-  const int n_kv = kCausal ? qt + 1 : n_tiles;
+  int j_first, j_last;  // key tiles this query tile's band reaches
+  band_key_tiles(q0, kTile, kTile, n_tiles, wl, wr, j_first, j_last);
+  const int n_kv = j_last - j_first + 1;
 
   if (tid == 0) {
     mbar_init(&s.qdo_full, 1);
@@ -853,12 +876,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (j >= 1 && !mbar_wait(&s.k_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, j * kTile, hh, bb);
+          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64,
+                      (j_first + j) * kTile, hh, bb);
         issued = 2 * j + 1;
         if (j >= 1 && !mbar_wait(&s.v_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.v_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, j * kTile, hh, bb);
+          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64,
+                      (j_first + j) * kTile, hh, bb);
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
@@ -919,6 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const long long srow = static_cast<long long>(bh) * Npad + i;
     const float lse2 = p.lse[srow];
     const float dii = p.di[srow];
+    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       if (!warp_wait(&s.s_full, j & 1, p.err, abort_flag)) {
@@ -930,8 +956,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      const int k0 = j * kTile;
-      const bool diag = kCausal && (k0 == q0);
+      const int k0 = (j_first + j) * kTile;
+      const bool cut = band_cuts(q0, kTile, k0, kTile, wl, wr);
 #pragma unroll 1
       for (int c = 0; c < kTile / 32; ++c) {
         uint32_t sr[32], dr[32];
@@ -939,17 +965,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tmem_ld32(tdP + lane_off + c * 32, dr);
         tmem_ld_wait();
         uint32_t dk[16];
+        if (!cut && !kAlibi) {
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float d2[2];
+          for (int t = 0; t < 32; t += 2) {
+            float d2[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + t + e;  // key index within the tile
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -lse2));
-            if (diag && col > r) pe = 0.f;
-            d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
+            for (int e = 0; e < 2; ++e) {
+              const float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -lse2));
+              d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
+            }
+            dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
           }
-          dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            float d2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = c * 32 + t + e;  // key index within the tile
+              float z = fmaf(__uint_as_float(sr[t + e]), sl2, -lse2);
+              if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(k0 + col - i)), z);
+              float pe = ex2_approx(z);
+              if (cut && !band_visible(i, k0 + col, wl, wr)) pe = 0.f;
+              d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
+            }
+            dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
+          }
         }
         store_row_chunk_sw128(s.ds, r, c, dk);
       }
@@ -1042,9 +1083,9 @@ cudaError_t set_smem(K kern, int bytes, bool& configured) {
   return e;
 }
 
-template <int D, bool kBf16, bool kCausal, bool kAtomic>
+template <int D, bool kBf16, bool kAlibi, bool kAtomic>
 cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_kernel<D, kBf16, kCausal, kAtomic>;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAlibi, kAtomic>;
   const int smem = static_cast<int>(sizeof(DkdvSmem<D>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
@@ -1055,9 +1096,9 @@ cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kAlibi>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dq_kernel<D, kBf16, kCausal>;
+  auto kern = bwd_dq_kernel<D, kBf16, kAlibi>;
   const int smem = static_cast<int>(sizeof(DqSmem<D>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
@@ -1068,9 +1109,9 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <bool kBf16, bool kCausal, bool kAtomic>
+template <bool kBf16, bool kAlibi, bool kAtomic>
 cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_d128_kernel<kBf16, kCausal, kAtomic>;
+  auto kern = bwd_dkdv_d128_kernel<kBf16, kAlibi, kAtomic>;
   const int smem = static_cast<int>(sizeof(Dkdv128Smem)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
@@ -1084,12 +1125,13 @@ cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
 template <int D, bool kBf16>
 cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
   const bool atomic = a.dq_accum != nullptr;
+  const bool alibi = a.band.alibi != nullptr;
   if (D == 128) {
-    if (a.causal)
+    if (alibi)
       return atomic ? launch_dkdv128_t<kBf16, true, true>(a, st) : launch_dkdv128_t<kBf16, true, false>(a, st);
     return atomic ? launch_dkdv128_t<kBf16, false, true>(a, st) : launch_dkdv128_t<kBf16, false, false>(a, st);
   }
-  if (a.causal)
+  if (alibi)
     return atomic ? launch_dkdv_t<D, kBf16, true, true>(a, st) : launch_dkdv_t<D, kBf16, true, false>(a, st);
   return atomic ? launch_dkdv_t<D, kBf16, false, true>(a, st) : launch_dkdv_t<D, kBf16, false, false>(a, st);
 }
@@ -1122,12 +1164,13 @@ cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t st) {
+  const bool alibi = a.band.alibi != nullptr;
   if (a.D == 64) {
-    if (a.bf16) return a.causal ? launch_dq_t<64, true, true>(a, st) : launch_dq_t<64, true, false>(a, st);
-    return a.causal ? launch_dq_t<64, false, true>(a, st) : launch_dq_t<64, false, false>(a, st);
+    if (a.bf16) return alibi ? launch_dq_t<64, true, true>(a, st) : launch_dq_t<64, true, false>(a, st);
+    return alibi ? launch_dq_t<64, false, true>(a, st) : launch_dq_t<64, false, false>(a, st);
   }
-  if (a.bf16) return a.causal ? launch_dq_t<128, true, true>(a, st) : launch_dq_t<128, true, false>(a, st);
-  return a.causal ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
+  if (a.bf16) return alibi ? launch_dq_t<128, true, true>(a, st) : launch_dq_t<128, true, false>(a, st);
+  return alibi ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
 }
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N, int H,

@@ -32,13 +32,17 @@
 // P then stays below 256, and O / l and the LSE are unchanged because both
 // use the same m.  Rows whose maximum barely moves never touch O in TMEM.
 //
-// Causal mask (walkthrough sec. 5.3): query i sees keys j <= i.  Key tiles
-// past a query tile's diagonal are never multiplied; the diagonal tile and a
-// ragged last tile are masked element-wise.  The grid runs head-major, the
-// longest query-tile pairs of a head first, so the CTAs in flight share one
-// head's K and V in L2.
+// Visible keys (fa_band.cuh): query i sees keys i - left .. i + right, the
+// causal mask (walkthrough sec. 5.3) being right = 0.  Each query tile
+// multiplies only the key tiles its band reaches; tiles the band cuts, and a
+// ragged last tile, are masked element-wise.  The pair's two tiles share one
+// K/V stream over the union of their key-tile ranges.  With an ALiBi slope
+// (flash_attn_func alibi_slopes) every score gets -slope * |i - j| added
+// before the softmax.  The grid runs head-major, the longest query-tile
+// pairs of a head first, so the CTAs in flight share one head's K and V in L2.
 #include <climits>
 
+#include "fa_band.cuh"
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 
@@ -71,7 +75,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kAlibi>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
   using Smem = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -83,18 +87,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   const int n_pairs = (n_q_tiles + 1) / 2;
   const int bh = static_cast<int>(blockIdx.x / n_pairs);
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
-  const int pt = kCausal ? n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs)
-                         : static_cast<int>(blockIdx.x % n_pairs);
+  const int wl = p.band.win_left, wr = p.band.win_right;
+  // With keys bounded on the right only (causal), later pairs see more keys:
+  // they go first.
+  const bool later_longer = wl < 0 && wr >= 0;
+  const int pt = later_longer ? n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs)
+                              : static_cast<int>(blockIdx.x % n_pairs);
   const int n_kv = (p.N + kTile - 1) / kTile;
-  // key tiles each query tile multiplies (0 when tile B lies past the end)
-  int n_of[2];
+  // Key tiles [lo_t, hi_t] each query tile multiplies (empty, lo > hi, when
+  // tile B lies past the end).  lo and hi never decrease from A to B, and
+  // each range holds the tile's diagonal, so their union is contiguous.
+  int lo[2], hi[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * pt + t;
-    n_of[t] = qt >= n_q_tiles ? 0 : (kCausal ? min(n_kv, qt + 1) : n_kv);
+    if (qt >= n_q_tiles) {
+      lo[t] = 1;
+      hi[t] = 0;
+    } else {
+      band_key_tiles(qt * kTile, kTile, kTile, n_kv, wl, wr, lo[t], hi[t]);
+    }
   }
-  const int n_max = max(n_of[0], n_of[1]);
-  const int n_q_here = n_of[1] > 0 ? 2 : 1;
+  const int j_first = lo[0], j_last = max(hi[0], hi[1]);
+  const int n_q_here = hi[1] >= lo[1] ? 2 : 1;
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
@@ -120,7 +135,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
-
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -133,23 +147,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full, kb * 64,
                       (2 * pt + t) * kTile, hh, bb);
       int issued = 0;
-      for (int j = 0; j < n_max; ++j) {
-        const int st = j & 1;
-        const uint32_t u = static_cast<uint32_t>(j >> 1);
-        if (j >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
+      for (int j = j_first; j <= j_last; ++j) {
+        const int jj = j - j_first;  // position in the stream
+        const int st = jj & 1;
+        const uint32_t u = static_cast<uint32_t>(jj >> 1);
+        if (jj >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
           tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st], kb * 64,
                       j * kTile, hh, bb);
-        if (j >= 2 && !mbar_wait(&s.v_empty[st], (u - 1) & 1, p.err, abort_flag)) {
-          issued = j * 2 + 1;
+        if (jj >= 2 && !mbar_wait(&s.v_empty[st], (u - 1) & 1, p.err, abort_flag)) {
+          issued = jj * 2 + 1;
           break;
         }
         mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
           tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
                       j * kTile, hh, bb);
-        issued = j * 2 + 2;
+        issued = jj * 2 + 2;
       }
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's smem goes away.
@@ -175,7 +190,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       // S_t(j) = Q_t K_j^T into tile t's S columns
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = desc_add(dq0, t * Smem::kTileBytes);
-        const uint64_t dk = desc_add(dk0, (j & 1) * Smem::kTileBytes);
+        const uint64_t dk = desc_add(dk0, ((j - j_first) & 1) * Smem::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
@@ -188,20 +203,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 mbar_wait(&s.k_full[0], 0, p.err, abort_flag);
       if (ok) {
         tc_fence_after();
+#pragma unroll
         for (int t = 0; t < 2; ++t)
-          if (n_of[t] > 0) issue_s(t, 0);
+          if (lo[t] == j_first && lo[t] <= hi[t]) issue_s(t, j_first);
         tc_commit(&s.k_empty[0]);
       }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int st = j & 1;
-        const uint32_t u = static_cast<uint32_t>(j >> 1);
-        if (!mbar_wait(&s.v_full[st], u & 1, p.err, abort_flag)) break;
+      for (int j = j_first; ok && j <= j_last; ++j) {
+        const int jj = j - j_first;
+        const int st = jj & 1;
+        if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
         bool k_next = false;  // K_{j+1} has landed
-        for (int t = 0; ok && t < 2; ++t) {
-          if (j >= n_of[t]) continue;
-          if (!mbar_wait(&s.p_full[t], j & 1, p.err, abort_flag)) {
+        // S_t(j+1) for tile t; its first S when the tile starts at j + 1
+        auto next_s = [&](int t) {
+          if (!k_next) {
+            const int jn = jj + 1;
+            if (!mbar_wait(&s.k_full[jn & 1], (jn >> 1) & 1, p.err, abort_flag)) return false;
+            tc_fence_after();
+            k_next = true;
+          }
+          issue_s(t, j + 1);
+          return true;
+        };
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {  // unrolled: lo[t], hi[t] stay in registers
+          if (!ok || j < lo[t] || j > hi[t]) continue;
+          if (!mbar_wait(&s.p_full[t], (j - lo[t]) & 1, p.err, abort_flag)) {
             ok = false;
-            break;
+            continue;
           }
           tc_fence_after();
           // O_t += P_t(j) V_j, with P read from tile t's S columns
@@ -209,22 +237,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
-                      desc_add(dv, kk * 16 * 128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                      desc_add(dv, kk * 16 * 128), idPV, (j > lo[t] || kk > 0) ? 1u : 0u);
           tc_commit(&s.o_done[t]);
-          if (j + 1 < n_of[t]) {
-            if (!k_next) {
-              if (!mbar_wait(&s.k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next = true;
-            }
-            issue_s(t, j + 1);  // S_t(j+1) follows the PV product that read P_t(j)
-          }
+          // S_t(j+1) follows the PV product that read P_t(j)
+          if (j + 1 <= hi[t] && !next_s(t)) ok = false;
         }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && lo[t] == j + 1 && lo[t] <= hi[t] && !next_s(t)) ok = false;
         tc_commit(&s.v_empty[st]);
-        if (k_next) tc_commit(&s.k_empty[(j + 1) & 1]);
+        if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
       }
       // Every MMA issued above completes before TMEM is released.
       tc_commit(&s.drain);
@@ -237,7 +259,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const int r = tid & 127;          // row within the tile and TMEM lane
     const int q0 = (2 * pt + t) * kTile;
     const int i = q0 + r;
-    const int n_tiles = n_of[t];
+    const int t_lo = t ? lo[1] : lo[0];
+    const int n_tiles = max(0, (t ? hi[1] : hi[0]) - t_lo + 1);
+    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + t * 128, tO = tbase + 256 + t * D;
     const float sl2 = p.scale_log2;
@@ -245,8 +269,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     float m = -INFINITY;  // reference maximum, log2 units
     float l = 0.f;        // running sum of 2^(t - m)
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s.s_full[t], j & 1, p.err, abort_flag)) {
+    for (int jj = 0; jj < n_tiles; ++jj) {
+      const int j = t_lo + jj;
+      if (!warp_wait(&s.s_full[t], jj & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
@@ -263,19 +288,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
           for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(raw[c][e]);
       }
-      // Scores -> log2 units.  With a positive scale this is folded into the
-      // exponent below (one FFMA per score); otherwise scale first.
-      if (!pos_scale) {
+      // Scores -> log2 units.  With a positive scale and no bias this is
+      // folded into the exponent below (one packed FMA per two scores);
+      // otherwise scale (and add the ALiBi bias) first.
+      const int k0 = j * kTile;
+      const bool prescale = kAlibi || !pos_scale;
+      if (kAlibi) {
+        const float d0 = static_cast<float>(k0 - i);  // key - query at column 0 (exact)
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          sv[c] = fmaf(sv[c], sl2, nslope2 * fabsf(d0 + static_cast<float>(c)));
+      } else if (!pos_scale) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c) sv[c] *= sl2;
       }
-      const int k0 = j * kTile;
-      const bool diag = kCausal && (k0 + kTile - 1 > q0);
-      if (diag || k0 + kTile > p.N) {
-        const int last = (kCausal ? min(i, p.N - 1) : p.N - 1) - k0;  // last visible column
+      if (band_cuts(q0, kTile, k0, kTile, p.band.win_left, p.band.win_right) ||
+          k0 + kTile > p.N) {
+        // this row's visible keys are first .. last
+        const int wl_ = p.band.win_left, wr_ = p.band.win_right;
+        const int first = wl_ < 0 ? 0 : i - wl_;
+        const int last = min(p.N - 1, wr_ < 0 ? p.N - 1 : i + wr_);
+        const int cf = first - k0, cl = last - k0;  // visible columns cf .. cl
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
-          if (c > last) sv[c] = -INFINITY;
+          if (c < cf || c > cl) sv[c] = -INFINITY;
       }
       // Row maximum: eight independent chains of three-input max.
       float mxs[8];
@@ -288,7 +324,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           mxs[e] = c + 8 < kTile ? fmax3(mxs[e], sv[c + e], sv[c + 8 + e]) : fmaxf(mxs[e], sv[c + e]);
       const float mx = fmax3(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], mxs[5]),
                              fmaxf(mxs[6], mxs[7]));
-      const float m_tile = pos_scale ? mx * sl2 : mx;
+      const float m_tile = prescale ? mx : mx * sl2;
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + kRescaleThreshold;
       float alpha = 1.f;
@@ -297,9 +333,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         l *= alpha;
         m = m_new;
       }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      if (jj > 0 && __any_sync(0xffffffffu, need)) {
         // O currently holds sum_{j' < j} P V; it must be final before scaling.
-        if (!warp_wait(&s.o_done[t], (j - 1) & 1, p.err, abort_flag)) {
+        if (!warp_wait(&s.o_done[t], (jj - 1) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -318,7 +354,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       // P = 2^(x * mult - m), two columns per packed FMA / add; the softmax
       // warps share issue slots with the MMA warp, so fewer instructions
       // here keep the tensor core fed.
-      const float mult = pos_scale ? sl2 : 1.f;
+      const float mult = prescale ? 1.f : sl2;
       const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
       uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
 #pragma unroll
@@ -390,9 +426,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   }
 }
 
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kAlibi>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, kBf16, kCausal>;
+  auto kern = fa_fwd_kernel<D, kBf16, kAlibi>;
   const int smem = static_cast<int>(sizeof(FwdSmem<D>)) + 1024;
   static bool configured = false;
   if (!configured) {
@@ -410,12 +446,13 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {
+  const bool alibi = a.band.alibi != nullptr;
   if (a.D == 64) {
-    if (a.bf16) return a.causal ? launch_fwd_t<64, true, true>(a, s) : launch_fwd_t<64, true, false>(a, s);
-    return a.causal ? launch_fwd_t<64, false, true>(a, s) : launch_fwd_t<64, false, false>(a, s);
+    if (a.bf16) return alibi ? launch_fwd_t<64, true, true>(a, s) : launch_fwd_t<64, true, false>(a, s);
+    return alibi ? launch_fwd_t<64, false, true>(a, s) : launch_fwd_t<64, false, false>(a, s);
   }
-  if (a.bf16) return a.causal ? launch_fwd_t<128, true, true>(a, s) : launch_fwd_t<128, true, false>(a, s);
-  return a.causal ? launch_fwd_t<128, false, true>(a, s) : launch_fwd_t<128, false, false>(a, s);
+  if (a.bf16) return alibi ? launch_fwd_t<128, true, true>(a, s) : launch_fwd_t<128, true, false>(a, s);
+  return alibi ? launch_fwd_t<128, false, true>(a, s) : launch_fwd_t<128, false, false>(a, s);
 }
 
 }  // namespace fa

@@ -13,12 +13,23 @@ constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 
 // Tensor maps are 4-D {D, N, H, B} over the caller's strides (D contiguous);
 // kernels address (batch, head) slice bh as head bh % H, batch bh / H.
+// Visible keys: query i sees key j when i - win_left <= j <= i + win_right,
+// a negative bound being absent; the causal mask is win_right = 0.  ALiBi:
+// the score of (i, j) gets -slope * |i - j| added, slope =
+// alibi[(bh / H) * alibi_bstride + bh % H] (alibi == nullptr: no bias).
+struct Band {
+  int win_left, win_right;
+  const float* alibi;
+  int alibi_bstride;
+};
+
 struct FwdLaunch {
   CUtensorMap map_q, map_k, map_v, map_o;  // box 64 x 128 x 1 x 1, 128B swizzle
   float* lse;                               // [BH][N]
   int N, BH, D, H;
   float scale_log2;                         // scale * log2(e)
-  int causal, bf16;
+  Band band;
+  int bf16;
   uint32_t* err;
 };
 
@@ -31,7 +42,8 @@ struct BwdLaunch {
   float* dq_accum;                          // [BH][N][D] or nullptr
   int N, BH, D, H;
   float scale, scale_log2;
-  int causal, bf16;
+  Band band;
+  int bf16;
   uint32_t* err;
 };
 

@@ -113,6 +113,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 }
 
 // ---------------------------------------------------------------------------
+// Per-warpgroup register budgets (every thread of the warpgroup executes the
+// same instruction).  The budgets of all warpgroups must add up to no more
+// than the block was launched with.
+// ---------------------------------------------------------------------------
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// ---------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------
 // Make generic-proxy writes to shared memory visible to the async proxy

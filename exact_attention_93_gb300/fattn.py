@@ -35,6 +35,12 @@ class FaLayout(ctypes.Structure):
     _fields_ = [(n, FaStrides) for n in ("q", "k", "v", "o", "dO", "dq", "dk", "dv")]
 
 
+class FaOptions(ctypes.Structure):
+    """fa_options: sliding window (-1 = no bound) and ALiBi slopes."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("alibi_slopes", ctypes.c_void_p), ("alibi_per_batch", ctypes.c_int)]
+
+
 class FattnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -88,6 +94,11 @@ def load(path: str | None = None):
                                    i, i, vp]),
             "fa_bwd_strided": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
                                    ctypes.POINTER(FaLayout), f, i, i, i, vp, sz, vp]),
+            "fa_fwd_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(FaLayout),
+                              ctypes.POINTER(FaOptions), f, i, i, vp]),
+            "fa_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
+                              ctypes.POINTER(FaLayout), ctypes.POINTER(FaOptions), f, i, i, i,
+                              vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -188,6 +199,50 @@ def fa_bwd_strided(q, k, v, o, lse, do, dq, dk, dv, layout: FaLayout, B: int, H:
                                int(bool(deterministic)), _ptr(workspace), workspace.numel(),
                                _stream(stream))
     _check(st, "fa_bwd_strided")
+
+
+def options(window=(-1, -1), alibi_slopes=None) -> FaOptions:
+    """fa_options for a window (left, right) and optional fp32 CUDA slopes of
+    shape [H] or [B, H] (kept alive by the caller until the call is done)."""
+    opt = FaOptions(int(window[0]), int(window[1]), None, 0)
+    if alibi_slopes is not None:
+        torch = _torch()
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda:
+            raise ValueError("alibi_slopes must be a float32 CUDA tensor")
+        if not alibi_slopes.is_contiguous() or alibi_slopes.dim() not in (1, 2):
+            raise ValueError("alibi_slopes must be a contiguous [H] or [B, H] tensor")
+        opt.alibi_slopes = alibi_slopes.data_ptr()
+        opt.alibi_per_batch = 1 if alibi_slopes.dim() == 2 else 0
+    return opt
+
+
+def fa_fwd_ex(q, k, v, o, lse, layout, opts, B: int, H: int, N: int, D: int, scale: float,
+              causal: bool, stream=None):
+    """fa_fwd_ex: layout (FaLayout or None for contiguous) and options
+    (FaOptions or None)."""
+    _check_cuda(q, k, v, o, lse)
+    st = load().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                          ctypes.byref(layout) if layout is not None else None,
+                          ctypes.byref(opts) if opts is not None else None,
+                          float(scale), int(bool(causal)), _dtype_code(q), _stream(stream))
+    _check(st, "fa_fwd_ex")
+
+
+def fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, layout, opts, B: int, H: int, N: int, D: int,
+              scale: float, causal: bool, deterministic: bool = False, workspace=None,
+              stream=None):
+    """fa_bwd_ex, matching fa_fwd_ex."""
+    _check_cuda(q, k, v, o, lse, do, dq, dk, dv, workspace)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, D, deterministic, q.device)
+    st = load().fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, H, N, D,
+                          ctypes.byref(layout) if layout is not None else None,
+                          ctypes.byref(opts) if opts is not None else None,
+                          float(scale), int(bool(causal)), _dtype_code(q),
+                          int(bool(deterministic)), _ptr(workspace), workspace.numel(),
+                          _stream(stream))
+    _check(st, "fa_bwd_ex")
 
 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):

@@ -91,6 +91,27 @@ typedef struct {
 } fa_layout;
 
 /*
+ * Options of flash_attn_func beyond causal ([API]):
+ *   window_left, window_right  sliding-window local attention: query i sees
+ *                              keys i - left .. i + right inclusive; -1 is
+ *                              no bound on that side, (-1, -1) is full
+ *                              attention.  Values below -1 are invalid.
+ *                              With causal != 0 the window is intersected
+ *                              with the causal mask.
+ *   alibi_slopes               NULL, or a device array of fp32 slopes, [H]
+ *                              (alibi_per_batch = 0) or [B, H] (= 1): the
+ *                              score of query i and key j gets
+ *                              -slope * |i - j| added after scaling.
+ *                              4-byte aligned; read by the kernels, not
+ *                              validated.
+ */
+typedef struct {
+  int window_left, window_right;
+  const float* alibi_slopes;
+  int alibi_per_batch;
+} fa_options;
+
+/*
  * Forward pass ([WALK] sec. 2.4 and 3.1; [DEEP] online softmax).
  *
  *   o[b,h,i,:]  = sum_j P_ij V[b,h,j,:],  P = softmax_j(scale * Q_i . K_j)
@@ -113,6 +134,16 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int D, const fa_layout* layout, float scale, int causal,
                          fa_dtype dtype, void* stream);
+
+/*
+ * The general forward: operands in `layout` (NULL: contiguous) and the
+ * window / ALiBi `options` (NULL: none).  fa_fwd and fa_fwd_strided are
+ * this with NULL options.  A bad window bound or a misaligned slope pointer
+ * returns FA_ERR_INVALID_ARG before anything is enqueued.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int D, const fa_layout* layout, const fa_options* options,
+                    float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
  * Workspace bytes fa_bwd needs, laid out as (each part 256-byte aligned):
@@ -156,6 +187,18 @@ fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void
                          int H, int N, int D, const fa_layout* layout, float scale, int causal,
                          fa_dtype dtype, int deterministic, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * The general backward, matching fa_fwd_ex: the same `layout` and
+ * `options` (and causal) as the forward that produced o and lse.  The
+ * gradients are those of the windowed, biased attention; the slopes get no
+ * gradient.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                    const fa_layout* layout, const fa_options* options, float scale, int causal,
+                    fa_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                    void* stream);
 
 /*
  * The stages fa_bwd enqueues, for callers that schedule or time them

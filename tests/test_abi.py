@@ -11,8 +11,8 @@ from exact_attention_93_gb300 import build, fattn
 NULL = None
 EXPECTED = [
     "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert", "fa_bwd_noalloc",
-    "fa_bwd_preprocess", "fa_bwd_strided", "fa_bwd_workspace_size", "fa_device_error", "fa_fwd",
-    "fa_fwd_strided", "fa_selftest_wait_timeout", "fa_status_string",
+    "fa_bwd_ex", "fa_bwd_preprocess", "fa_bwd_strided", "fa_bwd_workspace_size", "fa_device_error",
+    "fa_fwd", "fa_fwd_ex", "fa_fwd_strided", "fa_selftest_wait_timeout", "fa_status_string",
 ]
 
 
@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 2
+    assert lib.fa_abi_version() == 3
     names = [lib.fa_status_string(i).decode() for i in range(5)]
     assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
                      "FA_ERR_TIMEOUT"]
@@ -178,3 +178,20 @@ def test_strides_of_reads_named_dimensions():
     assert (s.batch, s.head, s.seq) == (5 * 3 * 4 * 128, 128, 3 * 4 * 128)
     with pytest.raises(ValueError):
         fattn.strides_of(x.transpose(2, 3), "bnhd")   # D not contiguous
+
+
+@pytest.mark.parametrize("win", [(-2, 0), (0, -2), (-5, -5)])
+def test_ex_entry_points_reject_bad_windows(lib, win):
+    opt = fattn.FaOptions(win[0], win[1], None, 0)
+    assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 128, 64, None, ctypes.byref(opt),
+                         ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_INVALID_ARG
+    need = lib.fa_bwd_workspace_size(1, 2, 128, 64, 0)
+    assert lib.fa_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 128, 64, None,
+                         ctypes.byref(opt), ctypes.c_float(0.125), 0, 0, 0, FAKE, need,
+                         NULL) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_ex_entry_points_reject_misaligned_slopes(lib):
+    opt = fattn.FaOptions(-1, -1, FAKE + 2, 0)
+    assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 128, 64, None, ctypes.byref(opt),
+                         ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_INVALID_ARG

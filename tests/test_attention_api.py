@@ -10,13 +10,20 @@ def x():
     return torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
 
 
-@pytest.mark.parametrize("kw", [{"dropout_p": 0.1}, {"window_size": (64, 0)},
-                                {"alibi_slopes": torch.ones(2)}])
-def test_unsupported_options_raise(kw):
+def test_dropout_raises():
     with pytest.raises(NotImplementedError):
+        flash_attn_func(x(), x(), x(), dropout_p=0.1)
+    with pytest.raises(NotImplementedError):
+        flash_attn_qkvpacked_func(torch.zeros(1, 128, 3, 2, 64, dtype=torch.bfloat16),
+                                  dropout_p=0.1)
+
+
+@pytest.mark.parametrize("kw", [{"window_size": (-2, 0)}, {"window_size": (3, -5)},
+                                {"alibi_slopes": torch.ones(3)},
+                                {"alibi_slopes": torch.ones(2, 2)}])
+def test_bad_window_or_slope_shapes_raise(kw):
+    with pytest.raises(ValueError):
         flash_attn_func(x(), x(), x(), **kw)
-    with pytest.raises(NotImplementedError):
-        flash_attn_qkvpacked_func(torch.zeros(1, 128, 3, 2, 64, dtype=torch.bfloat16), **kw)
 
 
 def test_packed_shape_is_checked():
