@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 mbar_wait(&s.k_full[0], 0, p.err, abort_flag);
       if (ok) {
         tc_fence_after();
-#pragma unroll
         for (int t = 0; t < 2; ++t)
           if (lo[t] == j_first && lo[t] <= hi[t]) issue_s(t, j_first);
         tc_commit(&s.k_empty[0]);
@@ -213,38 +212,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         const int st = jj & 1;
         if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
         bool k_next = false;  // K_{j+1} has landed
-        // S_t(j+1) for tile t; its first S when the tile starts at j + 1
-        auto next_s = [&](int t) {
-          if (!k_next) {
-            const int jn = jj + 1;
-            if (!mbar_wait(&s.k_full[jn & 1], (jn >> 1) & 1, p.err, abort_flag)) return false;
+        for (int t = 0; ok && t < 2; ++t) {
+          const int lt = t ? lo[1] : lo[0], ht = t ? hi[1] : hi[0];
+          const bool active = j >= lt && j <= ht;
+          // S_t(j+1) is next: after PV_t(j), or as the first product of a
+          // tile whose range starts at j + 1
+          const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
+          if (active) {
+            if (!mbar_wait(&s.p_full[t], (j - lt) & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            k_next = true;
-          }
-          issue_s(t, j + 1);
-          return true;
-        };
+            // O_t += P_t(j) V_j, with P read from tile t's S columns
+            const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {  // unrolled: lo[t], hi[t] stay in registers
-          if (!ok || j < lo[t] || j > hi[t]) continue;
-          if (!mbar_wait(&s.p_full[t], (j - lo[t]) & 1, p.err, abort_flag)) {
-            ok = false;
-            continue;
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
+                        desc_add(dv, kk * 16 * 128), idPV, (j > lt || kk > 0) ? 1u : 0u);
+            tc_commit(&s.o_done[t]);
           }
-          tc_fence_after();
-          // O_t += P_t(j) V_j, with P read from tile t's S columns
-          const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
-                      desc_add(dv, kk * 16 * 128), idPV, (j > lo[t] || kk > 0) ? 1u : 0u);
-          tc_commit(&s.o_done[t]);
-          // S_t(j+1) follows the PV product that read P_t(j)
-          if (j + 1 <= hi[t] && !next_s(t)) ok = false;
+          if (s_next) {
+            if (!k_next) {
+              if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, j + 1);  // after the PV product that read P_t(j)
+          }
         }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (ok && lo[t] == j + 1 && lo[t] <= hi[t] && !next_s(t)) ok = false;
         tc_commit(&s.v_empty[st]);
         if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
       }
