@@ -236,6 +236,62 @@ def run_reference(args, w):
     }), flush=True)
 
 
+def visible_pairs(N: int, causal: bool, left: int, right: int) -> int:
+    """(query, key) pairs the band lets through: query i sees keys
+    i - left .. i + right (-1: no bound), and j <= i when causal."""
+    import numpy as np
+    i = np.arange(N, dtype=np.int64)
+    lo = np.zeros(N, np.int64) if left < 0 else np.maximum(i - left, 0)
+    hi = np.full(N, N - 1, np.int64) if right < 0 else np.minimum(i + right, N - 1)
+    if causal:
+        hi = np.minimum(hi, i)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
+def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
+    """Forward + backward (atomic dQ) on the benchmark inputs with a sliding
+    window and with ALiBi, credited with the FLOPs of the visible pairs only
+    (4 D per pair forward, 2.5 times that backward)."""
+    import torch
+
+    from exact_attention_93_gb300 import fattn
+
+    B, H, N, D = w.B, w.H, w.N, w.D
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32,
+                          device=g["q"].device)
+    out = {}
+    for label, window, use_alibi in (("sliding window 4096", (4095, 0), False),
+                                     ("ALiBi", (-1, -1), True)):
+        opts = fattn.options(window, slopes if use_alibi else None)
+
+        def one():
+            fattn.fa_fwd_ex(g["q"], g["k"], g["v"], o, lse, None, opts, B, H, N, D, w.scale,
+                            w.causal)
+            fattn.fa_bwd_ex(g["q"], g["k"], g["v"], o, lse, g["do"], dq, dk, dv, None, opts,
+                            B, H, N, D, w.scale, w.causal, False, ws)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        s0.record(stream)
+        for _ in range(reps):
+            one()
+        e0.record(stream)
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(e0) / reps
+        pairs = visible_pairs(N, w.causal, *window)
+        flops = 3.5 * 4.0 * B * H * D * pairs
+        tf = flops / (ms * 1e-3) / 1e12
+        out[f"{w.describe()} fwd+bwd, {label}"] = {
+            "tflops": tf, "ms": ms, "frac_of_peak": tf / pk["sustained"],
+            "note": "FLOPs of the visible (query, key) pairs only; fa_fwd_ex + fa_bwd_ex"}
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the band runs")
+    return out
+
+
 def run_ours(args, w):
     import torch
 
@@ -391,6 +447,7 @@ def run_ours(args, w):
         extra[w2.describe() + " fwd"] = {"tflops": tf2, "ms": ms2,
                                          "frac_of_burst_peak": tf2 / pk["burst"],
                                          "note": "back-to-back launches; inputs 16.8 MB each fit in L2"}
+        extra.update(band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
