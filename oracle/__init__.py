@@ -62,6 +62,13 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_long, ctypes.c_long, ctypes.c_double, lp, ctypes.c_long,
         dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, dp, dp,
     ]
+    lib.fa_oracle_rows_bs.restype = ctypes.c_int
+    lib.fa_oracle_rows_bs.argtypes = [
+        dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.c_int, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.POINTER(ctypes.c_ubyte), ctypes.c_long, lp, ctypes.c_long,
+        dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, dp, dp,
+    ]
     lib.fa_oracle_threads.restype = ctypes.c_int
     lib.fa_oracle_threads.argtypes = []
     lib.fa_oracle_set_threads.restype = None
@@ -106,7 +113,8 @@ def _ptr(a):
 
 
 def attention_head(q, k, v, scale, causal, dout=None, rows=None,
-                   kv_range=None, want_grads=True, window=(-1, -1), alibi_slope=0.0):
+                   kv_range=None, want_grads=True, window=(-1, -1), alibi_slope=0.0,
+                   block_mask=None, block=128):
     """Exact attention for one (batch, head) slice.
 
     q, k, v, dout: [N, D].  rows: query-row indices (default: all rows).
@@ -114,7 +122,9 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
     when every row is requested, none otherwise).
     window: (left, right); query i sees keys i - left .. i + right, a
     negative bound being absent.  alibi_slope: the score of (i, j) gets
-    -alibi_slope * |i - j| added after scaling.
+    -alibi_slope * |i - j| added after scaling.  block_mask: None or a
+    [ceil(N / block), ceil(N / block)] array; key j is visible to query i
+    only where block_mask[i // block, j // block] is nonzero.
 
     Returns a dict with o [R, D], lse [R] and, when dout is given, dq [R, D],
     di [R] and (if a key range applies) dk, dv [end - begin, D].
@@ -147,13 +157,21 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
             dk = np.empty((ke - kb, D), np.float64)
             dv = np.empty((ke - kb, D), np.float64)
     left, right = (int(x) for x in window)
-    rc = lib.fa_oracle_rows_ex(
+    bm = None
+    if block_mask is not None:
+        nb = (N + block - 1) // block
+        bm = np.ascontiguousarray(np.asarray(block_mask) != 0, dtype=np.uint8)
+        if bm.shape != (nb, nb):
+            raise ValueError(f"block_mask must be [{nb}, {nb}] for N = {N}, block = {block}")
+    rc = lib.fa_oracle_rows_bs(
         _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, D, float(scale), int(bool(causal)),
         left, right, float(alibi_slope),
+        bm.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)) if bm is not None else None,
+        int(block),
         rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if rows_arr is not None else None,
         R, _ptr(o), _ptr(lse), _ptr(dq), _ptr(di), kb, ke, _ptr(dk), _ptr(dv))
     if rc != 0:
-        raise RuntimeError(f"fa_oracle_rows_ex failed with code {rc}")
+        raise RuntimeError(f"fa_oracle_rows_bs failed with code {rc}")
     out = {"o": o, "lse": lse}
     if dq is not None:
         out["dq"] = dq
@@ -165,12 +183,13 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
 
 
 def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None,
-              window=(-1, -1), alibi_slopes=None):
+              window=(-1, -1), alibi_slopes=None, block_mask=None, block=128):
     """Exact attention over a [B, H, N, D] batch, one (b, h) slice at a time.
 
     rows: None (every row) or a callable (b, h) -> row indices, or an array of
-    shape [B, H, R].  alibi_slopes: None, [H] or [B, H].  Returns arrays
-    shaped [B, H, R, ...]."""
+    shape [B, H, R].  alibi_slopes: None, [H] or [B, H].  block_mask: None,
+    [nb, nb] for every head, or [H, nb, nb].  Returns arrays shaped
+    [B, H, R, ...]."""
     B, H, N, D = tuple(q.shape)
     slopes = np.zeros((B, H))
     if alibi_slopes is not None:
@@ -187,7 +206,10 @@ def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None,
                 r = rows[b][h]
             one = attention_head(q[b, h], k[b, h], v[b, h], scale, causal,
                                  None if dout is None else dout[b, h], r,
-                                 kv_range, window=window, alibi_slope=slopes[b, h])
+                                 kv_range, window=window, alibi_slope=slopes[b, h],
+                                 block_mask=None if block_mask is None else
+                                 (block_mask[h] if np.ndim(block_mask) == 3 else block_mask),
+                                 block=block)
             for key, val in one.items():
                 res.setdefault(key, []).append(val)
     for key in list(res):

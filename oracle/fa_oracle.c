@@ -17,6 +17,9 @@
  *           introduction, flash_attn_func window_size)
  *   S_ij += -slope * |i - j|                              ALiBi bias on the
  *           scaled score (same page, alibi_slopes)
+ *   S_ij  = -inf unless mask[i / T][j / T] != 0           block-sparse
+ *           attention over T x T blocks (FlashAttention paper's block-sparse
+ *           extension, as the "FlashAttention 深入" and l189.com pages report it)
  *   m_i   = max_j S_ij
  *   P_ij  = exp(S_ij - m_i) / sum_k exp(S_ik - m_i)       max-shifted softmax
  *           (l189.com walkthrough, sec. 2.2 and sec. 5.2)
@@ -64,24 +67,34 @@ void fa_oracle_set_threads(int n) {
 
 /* One query row: materialise the score row S_i. and probability row P_i.,
  * then O_i, LSE_i and (if dout != NULL) dP_i., Di, dS_i. and dQ_i. */
+/* The block mask of one call: NULL, or one byte per (query block, key
+ * block) of `tile` x `tile` scores, n_kb key blocks per row of blocks. */
+typedef struct {
+    const unsigned char* mask;
+    long tile, n_kb;
+} block_mask;
+
 /* Is key j visible to query i? */
-static int visible(long i, long j, int causal, long left, long right) {
+static int visible(long i, long j, int causal, long left, long right,
+                   const block_mask* bm) {
     if (causal && j > i) return 0;
     if (left >= 0 && j < i - left) return 0;
     if (right >= 0 && j > i + right) return 0;
+    if (bm->mask && !bm->mask[(i / bm->tile) * bm->n_kb + j / bm->tile]) return 0;
     return 1;
 }
 
 static void one_row(const double* q, const double* k, const double* v,
                     const double* dout, long N, long D, double scale,
-                    int causal, long left, long right, double slope, long i,
+                    int causal, long left, long right, double slope,
+                    const block_mask* bm, long i,
                     double* s_row, double* p_row, double* ds_row, double* o_i,
                     double* lse_i, double* dq_i, double* di_i) {
     const double* qi = q + i * D;
 
     /* scores S_ij = scale * Q_i . K_j - slope * |i - j|, -inf where masked */
     for (long j = 0; j < N; ++j) {
-        if (!visible(i, j, causal, left, right)) {
+        if (!visible(i, j, causal, left, right, bm)) {
             s_row[j] = -INFINITY;
             continue;
         }
@@ -160,9 +173,23 @@ int fa_oracle_rows_ex(const double* q, const double* k, const double* v,
                       const long* rows, long nrows, double* o, double* lse,
                       double* dq, double* di, long kv_begin, long kv_end,
                       double* dk, double* dv) {
+    return fa_oracle_rows_bs(q, k, v, dout, N, D, scale, causal, left, right,
+                             slope, NULL, 1, rows, nrows, o, lse, dq, di,
+                             kv_begin, kv_end, dk, dv);
+}
+
+int fa_oracle_rows_bs(const double* q, const double* k, const double* v,
+                      const double* dout, long N, long D, double scale,
+                      int causal, long left, long right, double slope,
+                      const unsigned char* mask, long tile,
+                      const long* rows, long nrows, double* o, double* lse,
+                      double* dq, double* di, long kv_begin, long kv_end,
+                      double* dk, double* dv) {
     if (!q || !k || !v || !o || !lse || N < 1 || D < 1 || nrows < 0)
         return 1;
     if (left < -1 || right < -1 || !isfinite(slope)) return 1;
+    if (mask && tile < 1) return 1;
+    block_mask bm = {mask, tile, (N + tile - 1) / tile};
     if ((dq || di || dk || dv) && !dout) return 1;
     int want_cols = (dk != NULL) || (dv != NULL);
     if (want_cols && (kv_begin < 0 || kv_end > N || kv_begin > kv_end))
@@ -193,7 +220,7 @@ int fa_oracle_rows_ex(const double* q, const double* k, const double* v,
 #pragma omp parallel for schedule(dynamic, 1)
     for (long r = 0; r < nrows; ++r) {
         long i = rows ? rows[r] : r;
-        one_row(q, k, v, dout, N, D, scale, causal, left, right, slope, i,
+        one_row(q, k, v, dout, N, D, scale, causal, left, right, slope, &bm, i,
                 s_all + (size_t)r * N,
                 p_all + (size_t)r * N, dout ? ds_all + (size_t)r * N : NULL,
                 o + (size_t)r * D, lse + r, dq ? dq + (size_t)r * D : NULL,

@@ -44,6 +44,19 @@ int fa_oracle_rows_ex(const double* q, const double* k, const double* v,
                       double* dq, double* di, long kv_begin, long kv_end,
                       double* dk, double* dv);
 
+/*
+ * fa_oracle_rows_ex with a block mask: key j is visible to query i only when
+ * mask[(i / tile) * ceil(N / tile) + j / tile] != 0 (mask == NULL: every
+ * block).  A row that sees no key gets O = 0 and LSE = -inf, and no gradient.
+ */
+int fa_oracle_rows_bs(const double* q, const double* k, const double* v,
+                      const double* dout, long N, long D, double scale,
+                      int causal, long left, long right, double slope,
+                      const unsigned char* mask, long tile,
+                      const long* rows, long nrows, double* o, double* lse,
+                      double* dq, double* di, long kv_begin, long kv_end,
+                      double* dk, double* dv);
+
 /* OpenMP threads the next call will use, and a way to set them. */
 int fa_oracle_threads(void);
 void fa_oracle_set_threads(int n);

@@ -43,6 +43,10 @@ MUTANTS = [
     ("alibi without absolute value", "(double)labs(i - j)", "(double)(i - j)"),
     ("alibi scaled with the scores", "s_row[j] = scale * acc - slope * (double)labs(i - j);",
      "s_row[j] = scale * (acc - slope * (double)labs(i - j));"),
+    ("block mask ignored", "if (bm->mask && !bm->mask[(i / bm->tile) * bm->n_kb + j / bm->tile]) return 0;", ";"),
+    ("block mask transposed", "bm->mask[(i / bm->tile) * bm->n_kb + j / bm->tile]",
+     "bm->mask[(j / bm->tile) * bm->n_kb + i / bm->tile]"),
+    ("empty row divides by zero", "if (denom > 0.0)\n        for", "if (1)\n        for"),
 ]
 
 
@@ -64,6 +68,9 @@ def run_pins():
         ("alibi_bf", lambda: pins.test_window_and_alibi_brute_force(2, 3, 0.25, False)),
         ("band_sdpa", lambda: pins.test_window_and_alibi_match_torch_sdpa_float64(5, 3, 0.0, False)),
         ("alibi_closed", pins.test_alibi_at_zero_scale_is_a_closed_form),
+        ("blocks_bf", lambda: pins.test_block_mask_brute_force(9, 3, 2, False)),
+        ("blocks_sdpa", lambda: pins.test_block_mask_matches_torch_sdpa_float64(True)),
+        ("blocks_empty", pins.test_rows_that_see_no_key_are_zero_and_carry_no_gradient),
     ]
     for name, fn in checks:
         try:

@@ -571,3 +571,107 @@ def test_window_bounds_below_minus_one_are_rejected():
     q = rnd((4, 2), 107)
     with pytest.raises(RuntimeError):
         oracle.attention_head(q, q, q, 0.5, False, window=(-2, 0))
+
+
+# --------------------------------------------------------------------------
+# Block-sparse attention (the FlashAttention paper's block-sparse extension,
+# as the pages report it): scores outside the blocks a mask keeps are -inf
+# --------------------------------------------------------------------------
+
+def brute_force_blocks(q, k, v, scale, causal, mask, T):
+    """The definition with math.exp and an explicit block test; rows that see
+    nothing give O = 0 and LSE = -inf."""
+    n, d = q.shape
+    o = np.zeros((n, d))
+    lse = np.full(n, -np.inf)
+    for i in range(n):
+        s = [(j, scale * sum(q[i, t] * k[j, t] for t in range(d)))
+             for j in range(n) if (not causal or j <= i) and mask[i // T][j // T]]
+        if not s:
+            continue
+        z = sum(math.exp(val) for _, val in s)
+        lse[i] = math.log(z)
+        for j, val in s:
+            for t in range(d):
+                o[i, t] += math.exp(val) / z * v[j, t]
+    return o, lse
+
+
+def random_block_mask(nb, seed, density=0.5):
+    m = (np.random.default_rng(seed).random((nb, nb)) < density).astype(np.uint8)
+    return m
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n,T,seed", [(7, 2, 1), (9, 3, 2), (8, 4, 3), (10, 3, 4)])
+def test_block_mask_brute_force(n, T, seed, causal):
+    d = 3
+    q, k, v = rnd((n, d), 110 + seed), rnd((n, d), 111 + seed), rnd((n, d), 112 + seed)
+    nb = (n + T - 1) // T
+    mask = random_block_mask(nb, seed)
+    o_bf, lse_bf = brute_force_blocks(q, k, v, 0.8, causal, mask, T)
+    r = oracle.attention_head(q, k, v, 0.8, causal, block_mask=mask, block=T)
+    np.testing.assert_allclose(r["o"], o_bf, rtol=0, atol=1e-13)
+    np.testing.assert_array_equal(np.isinf(r["lse"]), np.isinf(lse_bf))
+    fin = np.isfinite(lse_bf)
+    np.testing.assert_allclose(r["lse"][fin], lse_bf[fin], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_matches_torch_sdpa_float64(causal):
+    """A mask that keeps every block row non-empty, against SDPA with the
+    block mask expanded to an additive -inf mask."""
+    n, d, T = 24, 8, 4
+    nb = n // T
+    mask = random_block_mask(nb, 7, 0.6)
+    np.fill_diagonal(mask, 1)
+    q, k, v, do = (rnd((n, d), s) for s in (120, 121, 122, 123))
+    scale = 1.0 / math.sqrt(d)
+    dense = np.kron(mask, np.ones((T, T))) > 0
+    if causal:
+        dense &= np.tril(np.ones((n, n), bool))
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    am = torch.tensor(np.where(dense, 0.0, -np.inf))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], attn_mask=am[None, None],
+        scale=scale)[0, 0]
+    out.backward(torch.tensor(do))
+    r = oracle.attention_head(q, k, v, scale, causal, dout=do, block_mask=mask, block=T)
+    np.testing.assert_allclose(r["o"], out.detach().numpy(), rtol=0, atol=1e-13)
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(r[name], t.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_block_diagonal_mask_is_attention_within_each_block():
+    n, d, T = 12, 4, 4
+    q, k, v, do = (rnd((n, d), s) for s in (124, 125, 126, 127))
+    r = oracle.attention_head(q, k, v, 0.6, False, dout=do, block_mask=np.eye(3), block=T)
+    for b in range(3):
+        sl = slice(b * T, (b + 1) * T)
+        one = oracle.attention_head(q[sl], k[sl], v[sl], 0.6, False, dout=do[sl])
+        for key in ("o", "lse", "dq", "dk", "dv"):
+            np.testing.assert_allclose(r[key][sl], one[key], rtol=0, atol=1e-14)
+
+
+def test_rows_that_see_no_key_are_zero_and_carry_no_gradient():
+    n, d, T = 8, 3, 4
+    q, k, v, do = (rnd((n, d), s) for s in (128, 129, 130, 131))
+    mask = np.array([[0, 0], [1, 1]])           # block row 0 sees nothing
+    r = oracle.attention_head(q, k, v, 0.7, False, dout=do, block_mask=mask, block=T)
+    assert np.all(r["o"][:4] == 0) and np.all(np.isneginf(r["lse"][:4]))
+    assert np.all(r["dq"][:4] == 0)
+    # the empty rows' dO does not reach dK, dV
+    do2 = do.copy()
+    do2[:4] += 5.0
+    r2 = oracle.attention_head(q, k, v, 0.7, False, dout=do2, block_mask=mask, block=T)
+    np.testing.assert_allclose(r2["dk"], r["dk"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(r2["dv"], r["dv"], rtol=0, atol=1e-14)
+
+
+def test_all_ones_block_mask_equals_no_mask():
+    n, d = 11, 4
+    q, k, v, do = (rnd((n, d), s) for s in (132, 133, 134, 135))
+    a = oracle.attention_head(q, k, v, 0.5, True, dout=do)
+    b = oracle.attention_head(q, k, v, 0.5, True, dout=do, block_mask=np.ones((4, 4)), block=3)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[key], b[key])
