@@ -248,9 +248,24 @@ def visible_pairs(N: int, causal: bool, left: int, right: int) -> int:
     return int(np.maximum(hi - lo + 1, 0).sum())
 
 
+def block_pairs(N: int, causal: bool, mask) -> int:
+    """(query, key) pairs inside the kept 128 x 128 blocks of `mask`
+    ([T, T], shared by every head), under the causal mask when asked."""
+    import numpy as np
+    T = mask.shape[0]
+    size = np.array([min(128, N - 128 * t) for t in range(T)], np.int64)
+    full = np.outer(size, size)
+    if causal:
+        # a diagonal block of s rows keeps s (s + 1) / 2 pairs; blocks above
+        # the diagonal keep none
+        full = np.tril(full, -1) + np.diag(size * (size + 1) // 2)
+    return int((full * (np.asarray(mask) != 0)).sum())
+
+
 def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
     """Forward + backward (atomic dQ) on the benchmark inputs with a sliding
-    window and with ALiBi, credited with the FLOPs of the visible pairs only
+    window, with ALiBi, and with a random block mask keeping half the blocks
+    (and the diagonal), credited with the FLOPs of the visible pairs only
     (4 D per pair forward, 2.5 times that backward)."""
     import torch
 
@@ -259,10 +274,20 @@ def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
     B, H, N, D = w.B, w.H, w.N, w.D
     slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32,
                           device=g["q"].device)
+    import numpy as np
+
+    T = (N + 127) // 128
+    rng = np.random.default_rng(0)
+    bmask = (rng.random((T, T)) < 0.5).astype(np.uint8)
+    np.fill_diagonal(bmask, 1)
+    bmask_dev = torch.tensor(bmask, device=g["q"].device)
     out = {}
-    for label, window, use_alibi in (("sliding window 4096", (4095, 0), False),
-                                     ("ALiBi", (-1, -1), True)):
-        opts = fattn.options(window, slopes if use_alibi else None)
+    for label, window, use_alibi, use_mask in (
+            ("sliding window 4096", (4095, 0), False, False),
+            ("ALiBi", (-1, -1), True, False),
+            ("block-sparse, half the 128 x 128 blocks", (-1, -1), False, True)):
+        opts = fattn.options(window, slopes if use_alibi else None,
+                             bmask_dev if use_mask else None)
 
         def one():
             fattn.fa_fwd_ex(g["q"], g["k"], g["v"], o, lse, None, opts, B, H, N, D, w.scale,
@@ -281,7 +306,7 @@ def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
         e0.record(stream)
         torch.cuda.synchronize()
         ms = s0.elapsed_time(e0) / reps
-        pairs = visible_pairs(N, w.causal, *window)
+        pairs = block_pairs(N, w.causal, bmask) if use_mask else visible_pairs(N, w.causal, *window)
         flops = 3.5 * 4.0 * B * H * D * pairs
         tf = flops / (ms * 1e-3) / 1e12
         out[f"{w.describe()} fwd+bwd, {label}"] = {

@@ -9,8 +9,10 @@ on the caller's tensors in place through the strided C ABI (fa_fwd_strided,
 fa_bwd_ex): no transposes or copies of Q, K, V.  window_size gives
 sliding-window local attention (query i sees keys i - left .. i + right,
 -1 meaning no bound) and alibi_slopes ([nheads] or [batch, nheads] fp32) adds
--slope * |i - j| to each score, as the page documents.  Dropout is not
-provided; asking for it raises.
+-slope * |i - j| to each score, as the page documents.  block_mask (an
+extension of that argument list) restricts attention to the kept blocks of
+128 x 128 scores: block-sparse attention.  Dropout is not provided; asking
+for it raises.
 """
 from __future__ import annotations
 
@@ -19,6 +21,16 @@ import torch
 from . import fattn
 
 __all__ = ["flash_attn_func", "flash_attn_qkvpacked_func"]
+
+
+def _check_block_mask(block_mask, N, H):
+    if block_mask is None:
+        return None
+    T = (N + 127) // 128
+    if tuple(block_mask.shape) not in ((T, T), (H, T, T)):
+        raise ValueError(f"block_mask must have shape ({T}, {T}) or ({H}, {T}, {T}) "
+                         "for blocks of 128 x 128 scores")
+    return block_mask.to(torch.uint8).contiguous()
 
 
 def _check_options(dropout_p, window_size, alibi_slopes, B, H):
@@ -53,29 +65,31 @@ def _layout(q, k, v, o, do=None, dq=None, dk=None, dv=None) -> fattn.FaLayout:
                           _bnhd(dk) if dk is not None else z, _bnhd(dv) if dv is not None else z)
 
 
-def _forward(q, k, v, scale, causal, window, slopes):
+def _forward(q, k, v, scale, causal, window, slopes, bmask):
     B, N, H, D = (int(x) for x in q.shape)
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k and v must have the same (batch, seqlen, nheads, headdim) shape")
     o = torch.empty((B, N, H, D), dtype=q.dtype, device=q.device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fattn.fa_fwd_ex(q, k, v, o, lse, _layout(q, k, v, o), fattn.options(window, slopes),
+    fattn.fa_fwd_ex(q, k, v, o, lse, _layout(q, k, v, o), fattn.options(window, slopes, bmask),
                     B, H, N, D, scale, causal)
     return o, lse
 
 
-def _backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, window, slopes, deterministic):
+def _backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, window, slopes, bmask,
+              deterministic):
     B, N, H, D = (int(x) for x in q.shape)
     fattn.fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, _layout(q, k, v, o, do, dq, dk, dv),
-                    fattn.options(window, slopes), B, H, N, D, scale, causal, deterministic)
+                    fattn.options(window, slopes, bmask), B, H, N, D, scale, causal,
+                    deterministic)
 
 
 class _FlashAttn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal, window, slopes, deterministic):
-        o, lse = _forward(q, k, v, scale, causal, window, slopes)
+    def forward(ctx, q, k, v, scale, causal, window, slopes, bmask, deterministic):
+        o, lse = _forward(q, k, v, scale, causal, window, slopes, bmask)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.slopes = slopes
+        ctx.slopes, ctx.bmask = slopes, bmask
         ctx.scale, ctx.causal, ctx.window, ctx.deterministic = scale, causal, window, deterministic
         ctx.mark_non_differentiable(lse)
         return o, lse
@@ -85,17 +99,17 @@ class _FlashAttn(torch.autograd.Function):
         q, k, v, o, lse = ctx.saved_tensors
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
-                  ctx.window, ctx.slopes, ctx.deterministic)
-        return dq, dk, dv, None, None, None, None, None
+                  ctx.window, ctx.slopes, ctx.bmask, ctx.deterministic)
+        return dq, dk, dv, None, None, None, None, None, None
 
 
 class _FlashAttnQKVPacked(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, qkv, scale, causal, window, slopes, deterministic):
+    def forward(ctx, qkv, scale, causal, window, slopes, bmask, deterministic):
         q, k, v = qkv.unbind(dim=2)
-        o, lse = _forward(q, k, v, scale, causal, window, slopes)
+        o, lse = _forward(q, k, v, scale, causal, window, slopes, bmask)
         ctx.save_for_backward(qkv, o, lse)
-        ctx.slopes = slopes
+        ctx.slopes, ctx.bmask = slopes, bmask
         ctx.scale, ctx.causal, ctx.window, ctx.deterministic = scale, causal, window, deterministic
         ctx.mark_non_differentiable(lse)
         return o, lse
@@ -107,36 +121,41 @@ class _FlashAttnQKVPacked(torch.autograd.Function):
         dqkv = torch.empty_like(qkv)
         dq, dk, dv = dqkv.unbind(dim=2)
         _backward(q, k, v, o, lse, _grad_operand(do), dq, dk, dv, ctx.scale, ctx.causal,
-                  ctx.window, ctx.slopes, ctx.deterministic)
-        return dqkv, None, None, None, None, None
+                  ctx.window, ctx.slopes, ctx.bmask, ctx.deterministic)
+        return dqkv, None, None, None, None, None, None
 
 
 def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=False,
                     window_size=(-1, -1), alibi_slopes=None, deterministic=False,
-                    return_lse=False):
+                    return_lse=False, block_mask=None):
     """Exact attention of q, k, v shaped (batch, seqlen, nheads, headdim),
     bf16 or fp16 CUDA tensors with headdim 64 or 128 contiguous.  Returns the
     output in the same shape (and the fp32 (batch, nheads, seqlen) log-sum-exp
     of the scaled, biased scores when return_lse).  window_size = (left,
     right) limits query i to keys i - left .. i + right (-1: no bound);
-    alibi_slopes adds -slope * |i - j|.  Differentiable in q, k, v (not in the
-    slopes); deterministic selects the two-pass dQ backward."""
+    alibi_slopes adds -slope * |i - j|.  block_mask ((T, T) or (nheads, T, T),
+    T = ceil(seqlen / 128)) keeps only the nonzero blocks of 128 x 128 scores.
+    Differentiable in q, k, v (not in the slopes); deterministic selects the
+    two-pass dQ backward."""
     window, slopes = _check_options(dropout_p, window_size, alibi_slopes, q.shape[0], q.shape[2])
+    bmask = _check_block_mask(block_mask, q.shape[1], q.shape[2])
     scale = q.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
-    o, lse = _FlashAttn.apply(q, k, v, scale, bool(causal), window, slopes, bool(deterministic))
+    o, lse = _FlashAttn.apply(q, k, v, scale, bool(causal), window, slopes, bmask,
+                              bool(deterministic))
     return (o, lse) if return_lse else o
 
 
 def flash_attn_qkvpacked_func(qkv, dropout_p=0.0, softmax_scale=None, causal=False,
                               window_size=(-1, -1), alibi_slopes=None, deterministic=False,
-                              return_lse=False):
+                              return_lse=False, block_mask=None):
     """flash_attn_func on one packed (batch, seqlen, 3, nheads, headdim)
     tensor; its gradient comes back in the same packed layout."""
     if qkv.dim() != 5 or qkv.shape[2] != 3:
         raise ValueError("expected qkv of shape (batch, seqlen, 3, nheads, headdim)")
     window, slopes = _check_options(dropout_p, window_size, alibi_slopes, qkv.shape[0],
                                     qkv.shape[3])
+    bmask = _check_block_mask(block_mask, qkv.shape[1], qkv.shape[3])
     scale = qkv.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
-    o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), window, slopes,
+    o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), window, slopes, bmask,
                                        bool(deterministic))
     return (o, lse) if return_lse else o

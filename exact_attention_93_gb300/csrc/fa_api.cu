@@ -101,8 +101,8 @@ fa_status check_strides(const Shape& s, const RowStrides& r) {
 
 // The band of visible keys: the window of `opt` (absent when opt is null)
 // intersected with the causal mask (right bound 0), and the ALiBi slopes.
-fa_status make_band(const fa_options* opt, int causal, int H, Band* b) {
-  *b = Band{-1, -1, nullptr, 0};
+fa_status make_band(const fa_options* opt, int causal, const Shape& sh, Band* b) {
+  *b = Band{-1, -1, nullptr, 0, nullptr, 0};
   if (opt) {
     if (opt->window_left < -1 || opt->window_right < -1) return FA_ERR_INVALID_ARG;
     if (opt->alibi_slopes && (reinterpret_cast<uintptr_t>(opt->alibi_slopes) & 3u) != 0)
@@ -110,7 +110,13 @@ fa_status make_band(const fa_options* opt, int causal, int H, Band* b) {
     b->win_left = opt->window_left;
     b->win_right = opt->window_right;
     b->alibi = opt->alibi_slopes;
-    b->alibi_bstride = opt->alibi_per_batch ? H : 0;
+    b->alibi_bstride = opt->alibi_per_batch ? sh.H : 0;
+    if (opt->block_mask) {
+      const long long nt = (sh.N + kTile - 1) / kTile;
+      if (nt > kMaxSparseTiles) return FA_ERR_UNSUPPORTED;
+      b->block_mask = opt->block_mask;
+      b->bm_head_stride = opt->block_mask_per_head ? nt * nt : 0;
+    }
   }
   if (causal) b->win_right = 0;  // j <= i, and j <= i + right for any right >= 0
   return FA_OK;
@@ -168,7 +174,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 3; }
+int fa_abi_version(void) { return 4; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -191,7 +197,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   fa_status st = check_shape(s, dtype);
   if (st != FA_OK) return st;
   Band band;
-  if ((st = make_band(opt, causal, s.H, &band)) != FA_OK) return st;
+  if ((st = make_band(opt, causal, s, &band)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
@@ -221,7 +227,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   fa_status st = check_shape(s, dtype);
   if (st != FA_OK) return st;
   Band band;
-  if ((st = make_band(opt, causal, s.H, &band)) != FA_OK) return st;
+  if ((st = make_band(opt, causal, s, &band)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -313,7 +319,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   if ((st = check_ws(s, deterministic, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
   Band band;
-  if ((st = make_band(nullptr, causal, H, &band)) != FA_OK) return st;
+  if ((st = make_band(nullptr, causal, s, &band)) != FA_OK) return st;
   if ((st = make_bwd_launch(&a, q, k, v, dO, nullptr, dk, dv, s, contiguous_layout(s), scale,
                             band, dtype, deterministic, workspace)) != FA_OK)
     return st;
@@ -332,7 +338,7 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
   if ((st = check_ws(s, 1, workspace, workspace_bytes)) != FA_OK) return st;
   BwdLaunch a;
   Band band;
-  if ((st = make_band(nullptr, causal, H, &band)) != FA_OK) return st;
+  if ((st = make_band(nullptr, causal, s, &band)) != FA_OK) return st;
   if ((st = make_bwd_launch(&a, q, k, v, dO, dq, nullptr, nullptr, s, contiguous_layout(s),
                             scale, band, dtype, 1, workspace)) != FA_OK)
     return st;

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 // ---------------------------------------------------------------------------
 // dK / dV (and atomic dQ)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kSparse>
 struct DkdvSmem {
   static constexpr int kBlocks = D / 64;
   static constexpr int kBlockBytes = kTile * 128;
@@ -137,11 +137,12 @@ struct DkdvSmem {
   uint64_t kv_full, qdo_full, qdo_empty, s_full, p_full, mma_done, tmem_free, drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t q_tiles[kSparse ? kMaxSparseTiles / 32 : 1];  // block-sparse: query tiles
 };
 
-template <int D, bool kBf16, bool kAlibi, bool kAtomicDq>
+template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdLaunch p) {
-  using Smem = DkdvSmem<D>;
+  using Smem = DkdvSmem<D, kSparse>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -156,7 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   const int wl = p.band.win_left, wr = p.band.win_right;
   int it_begin, it_last;  // query tiles whose band reaches this key tile
   band_query_tiles(k0, kTile, kTile, n_tiles, wl, wr, it_begin, it_last);
-  const int n_it = it_last - it_begin + 1;
+  const TileWalk<kSparse> walk{it_begin, it_last, n_tiles, TileSet{s.q_tiles, n_tiles}};
+  if constexpr (kSparse)
+    fill_tile_set(s.q_tiles, n_tiles, [&](int it) {
+      return it >= it_begin && it <= it_last && block_kept(p.band, bh, p.H, n_tiles, it, kt);
+    });
+  __syncthreads();
+  const int n_it = walk.count();
 
   if (tid == 0) {
     mbar_init(&s.kv_full, 1);
@@ -191,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
       }
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int q0 = (it_begin + it) * kTile;
+      for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
+        const int q0 = qt * kTile;
         if (it >= 1 && !mbar_wait(&s.qdo_empty, (it - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes + 2 * kTile * 4);
         for (int kb = 0; kb < Smem::kBlocks; ++kb) {
@@ -276,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     const float sl2 = p.scale_log2;
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int q0 = (it_begin + it) * kTile;
+    for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
+      const int q0 = qt * kTile;
       if (!warp_wait(&s.s_full, it & 1, p.err, abort_flag) ||
           !warp_wait(&s.qdo_full, it & 1, p.err, abort_flag)) {  // lse2 / Di of this tile
         ok = false;
@@ -361,16 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     }
 
     // ---------------------------------------------------------- epilogue
+    // A key tile the block mask leaves unseen has dK = dV = 0.
     bool done = ok;
-    if (ok && !kAtomicDq) done = warp_wait(&s.mma_done, (n_it - 1) & 1, p.err, abort_flag);
+    if (ok && !kAtomicDq && n_it > 0)
+      done = warp_wait(&s.mma_done, (n_it - 1) & 1, p.err, abort_flag);
     if (named_bar_and(1, 128, done)) {
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32], b[32];
-        tmem_ld32(tdV + lane_off + c * 32, a);
-        tmem_ld32(tdK + lane_off + c * 32, b);
-        tmem_ld_wait();
+        if (n_it > 0) {
+          tmem_ld32(tdV + lane_off + c * 32, a);
+          tmem_ld32(tdK + lane_off + c * 32, b);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
+        }
         uint32_t pa[16], pb[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -430,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 constexpr int kD128Threads = 480;  // warps 0-7 elementwise, 8-11 dQ, 12 producer, 13-14 MMA
 constexpr int kQ64 = 64;
 
+template <bool kSparse>
 struct Dkdv128Smem {
   static constexpr int kKBlock = kTile * 128;  // 128 rows x 128 B
   static constexpr int kQBlock = kQ64 * 128;   // 64 rows x 128 B
@@ -444,13 +459,14 @@ struct Dkdv128Smem {
   uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t q_tiles[kSparse ? 2 * kMaxSparseTiles / 32 : 1];  // block-sparse: 64-row query tiles
 };
 
-template <bool kBf16, bool kAlibi, bool kAtomicDq>
+template <bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
 __global__ void __launch_bounds__(kD128Threads, 1)
     bwd_dkdv_d128_kernel(const __grid_constant__ BwdLaunch p) {
   constexpr int D = 128;
-  using Smem = Dkdv128Smem;
+  using Smem = Dkdv128Smem<kSparse>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -467,7 +483,13 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   const int wl = p.band.win_left, wr = p.band.win_right;
   int it_begin, it_last;  // 64-row query tiles whose band reaches this key tile
   band_query_tiles(k0, kTile, kQ64, n_q64, wl, wr, it_begin, it_last);
-  const int n_it = it_last - it_begin + 1;
+  const TileWalk<kSparse> walk{it_begin, it_last, n_q64, TileSet{s.q_tiles, n_q64}};
+  if constexpr (kSparse)  // the mask's 128-row blocks hold 64-row tiles 2b, 2b + 1
+    fill_tile_set(s.q_tiles, n_q64, [&](int it) {
+      return it >= it_begin && it <= it_last && block_kept(p.band, bh, p.H, n_kt, it >> 1, kt);
+    });
+  __syncthreads();
+  const int n_it = walk.count();
 
   if (tid == 0) {
     mbar_init(&s.kv_full, 1);
@@ -509,10 +531,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         tma_load_4d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
       }
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
         const int st = it % 3;
         if (it >= 3 && !mbar_wait(&s.qdo_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
-        const int q0 = (it_begin + it) * kQ64;
+        const int q0 = qt * kQ64;
         mbar_arrive_expect_tx(&s.qdo_full[st], 4 * Smem::kQBlock + 2 * kQ64 * 4);
         for (int kb = 0; kb < 2; ++kb) {
           tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, hh, bb);
@@ -616,7 +638,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it and the last dS^T is in shared memory.
-      if (ok && kAtomicDq && !*abort_flag) {
+      if (ok && kAtomicDq && !*abort_flag && n_it > 0) {
         const int j = n_it - 1;
         if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
             (j < 2 ||
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       const int quad = warp & 3;
       const int d = quad * 32 + lane;  // TMEM lane = column d of dQ
       const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-      for (int j = 0; j < n_it; ++j) {
+      for (int j = 0, qt = walk.first(); j < n_it; ++j, qt = walk.next(qt)) {
         if (!warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const int b = (j + 1) & 1;  // dQ^T(j) sits in the S^T columns of tile j + 1
@@ -648,7 +670,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&s.tmem_free[b]);
-        const int q0 = (it_begin + j) * kQ64;
+        const int q0 = qt * kQ64;
         float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
         const int nq = min(kQ64, p.N - q0);
 #pragma unroll
@@ -667,9 +689,9 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     const float sl2 = p.scale_log2;
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
       const int b = it & 1, st = it % 3;
-      const int q0 = (it_begin + it) * kQ64;
+      const int q0 = qt * kQ64;
       // S^T(it) was issued after dV, dK(it - 2), the last readers of the
       // P^T / dS^T columns of buffer b, had completed.
       if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) ||
@@ -767,9 +789,14 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       for (int c = 0; c < 2; ++c) {  // this warp's 64 d columns, 32 at a time
         const int c32 = half * 2 + c;
         uint32_t a[32], g[32];
-        tmem_ld32(tdV + lane_off + c32 * 32, a);
-        tmem_ld32(tdK + lane_off + c32 * 32, g);
-        tmem_ld_wait();
+        if (n_it > 0) {
+          tmem_ld32(tdV + lane_off + c32 * 32, a);
+          tmem_ld32(tdK + lane_off + c32 * 32, g);
+          tmem_ld_wait();
+        } else {  // a key tile the block mask leaves unseen: dK = dV = 0
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+        }
         uint32_t pa[16], pb[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -804,7 +831,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
 // ---------------------------------------------------------------------------
 // deterministic dQ
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kSparse>
 struct DqSmem {
   static constexpr int kBlocks = D / 64;
   static constexpr int kBlockBytes = kTile * 128;
@@ -817,11 +844,12 @@ struct DqSmem {
   uint64_t qdo_full, k_full, k_empty, v_full, v_empty, s_full, p_full, mma_done, drain;
   uint32_t tmem_base;
   int abort_flag;
+  uint32_t k_tiles[kSparse ? kMaxSparseTiles / 32 : 1];  // block-sparse: key tiles
 };
 
-template <int D, bool kBf16, bool kAlibi>
+template <int D, bool kBf16, bool kAlibi, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdLaunch p) {
-  using Smem = DqSmem<D>;
+  using Smem = DqSmem<D, kSparse>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -838,7 +866,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   const int q0 = qt * kTile;
   int j_first, j_last;  // key tiles this query tile's band reaches
   band_key_tiles(q0, kTile, kTile, n_tiles, wl, wr, j_first, j_last);
-  const int n_kv = j_last - j_first + 1;
+  const TileWalk<kSparse> walk{j_first, j_last, n_tiles, TileSet{s.k_tiles, n_tiles}};
+  if constexpr (kSparse)
+    fill_tile_set(s.k_tiles, n_tiles, [&](int j) {
+      return j >= j_first && j <= j_last && block_kept(p.band, bh, p.H, n_tiles, qt, j);
+    });
+  __syncthreads();
+  const int n_kv = walk.count();
 
   if (tid == 0) {
     mbar_init(&s.qdo_full, 1);
@@ -872,18 +906,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tma_load_4d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, hh, bb);
       }
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0, kt = walk.first(); j < n_kv; ++j, kt = walk.next(kt)) {
         if (j >= 1 && !mbar_wait(&s.k_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64,
-                      (j_first + j) * kTile, hh, bb);
+          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, kt * kTile,
+                      hh, bb);
         issued = 2 * j + 1;
         if (j >= 1 && !mbar_wait(&s.v_empty, (j - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.v_full, Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64,
-                      (j_first + j) * kTile, hh, bb);
+          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, kt * kTile,
+                      hh, bb);
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
@@ -946,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const float dii = p.di[srow];
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0, kt = walk.first(); j < n_kv; ++j, kt = walk.next(kt)) {
       if (!warp_wait(&s.s_full, j & 1, p.err, abort_flag)) {
         ok = false;
         break;
@@ -956,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      const int k0 = (j_first + j) * kTile;
+      const int k0 = kt * kTile;
       const bool cut = band_cuts(q0, kTile, k0, kTile, wl, wr);
 #pragma unroll 1
       for (int c = 0; c < kTile / 32; ++c) {
@@ -998,14 +1032,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       tc_fence_before();
       mbar_arrive(&s.p_full);
     }
-    const bool mine = ok && warp_wait(&s.mma_done, (n_kv - 1) & 1, p.err, abort_flag);
+    // A query tile the block mask leaves without keys has dQ = 0; its Q
+    // tile, the output stage, must have landed before it is overwritten.
+    const bool mine =
+        ok && (n_kv > 0 ? warp_wait(&s.mma_done, (n_kv - 1) & 1, p.err, abort_flag)
+                        : warp_wait(&s.qdo_full, 0, p.err, abort_flag));
     if (named_bar_and(1, 128, mine)) {
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t g[32];
-        tmem_ld32(tdQ + lane_off + c * 32, g);
-        tmem_ld_wait();
+        if (n_kv > 0) {
+          tmem_ld32(tdQ + lane_off + c * 32, g);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) g[e] = 0u;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t)
@@ -1083,10 +1126,10 @@ cudaError_t set_smem(K kern, int bytes, bool& configured) {
   return e;
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kAtomic>
+template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
 cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAlibi, kAtomic>;
-  const int smem = static_cast<int>(sizeof(DkdvSmem<D>)) + 1024;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
+  const int smem = static_cast<int>(sizeof(DkdvSmem<D, kSparse>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
@@ -1096,10 +1139,10 @@ cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool kBf16, bool kAlibi>
+template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dq_kernel<D, kBf16, kAlibi>;
-  const int smem = static_cast<int>(sizeof(DqSmem<D>)) + 1024;
+  auto kern = bwd_dq_kernel<D, kBf16, kAlibi, kSparse>;
+  const int smem = static_cast<int>(sizeof(DqSmem<D, kSparse>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
@@ -1109,10 +1152,10 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <bool kBf16, bool kAlibi, bool kAtomic>
+template <bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
 cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_d128_kernel<kBf16, kAlibi, kAtomic>;
-  const int smem = static_cast<int>(sizeof(Dkdv128Smem)) + 1024;
+  auto kern = bwd_dkdv_d128_kernel<kBf16, kAlibi, kAtomic, kSparse>;
+  const int smem = static_cast<int>(sizeof(Dkdv128Smem<kSparse>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
@@ -1122,18 +1165,36 @@ cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool kBf16>
-cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
+template <int D, bool kBf16, bool kSparse>
+cudaError_t launch_dkdv_ds(const BwdLaunch& a, cudaStream_t st) {
   const bool atomic = a.dq_accum != nullptr;
   const bool alibi = a.band.alibi != nullptr;
   if (D == 128) {
     if (alibi)
-      return atomic ? launch_dkdv128_t<kBf16, true, true>(a, st) : launch_dkdv128_t<kBf16, true, false>(a, st);
-    return atomic ? launch_dkdv128_t<kBf16, false, true>(a, st) : launch_dkdv128_t<kBf16, false, false>(a, st);
+      return atomic ? launch_dkdv128_t<kBf16, true, true, kSparse>(a, st)
+                    : launch_dkdv128_t<kBf16, true, false, kSparse>(a, st);
+    return atomic ? launch_dkdv128_t<kBf16, false, true, kSparse>(a, st)
+                  : launch_dkdv128_t<kBf16, false, false, kSparse>(a, st);
   }
   if (alibi)
-    return atomic ? launch_dkdv_t<D, kBf16, true, true>(a, st) : launch_dkdv_t<D, kBf16, true, false>(a, st);
-  return atomic ? launch_dkdv_t<D, kBf16, false, true>(a, st) : launch_dkdv_t<D, kBf16, false, false>(a, st);
+    return atomic ? launch_dkdv_t<D, kBf16, true, true, kSparse>(a, st)
+                  : launch_dkdv_t<D, kBf16, true, false, kSparse>(a, st);
+  return atomic ? launch_dkdv_t<D, kBf16, false, true, kSparse>(a, st)
+                : launch_dkdv_t<D, kBf16, false, false, kSparse>(a, st);
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_dkdv_d(const BwdLaunch& a, cudaStream_t st) {
+  return a.band.block_mask ? launch_dkdv_ds<D, kBf16, true>(a, st)
+                           : launch_dkdv_ds<D, kBf16, false>(a, st);
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_dq_d(const BwdLaunch& a, cudaStream_t st) {
+  const bool alibi = a.band.alibi != nullptr;
+  if (a.band.block_mask)
+    return alibi ? launch_dq_t<D, kBf16, true, true>(a, st) : launch_dq_t<D, kBf16, false, true>(a, st);
+  return alibi ? launch_dq_t<D, kBf16, true, false>(a, st) : launch_dq_t<D, kBf16, false, false>(a, st);
 }
 
 }  // namespace
@@ -1164,13 +1225,8 @@ cudaError_t launch_bwd_dkdv(const BwdLaunch& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t st) {
-  const bool alibi = a.band.alibi != nullptr;
-  if (a.D == 64) {
-    if (a.bf16) return alibi ? launch_dq_t<64, true, true>(a, st) : launch_dq_t<64, true, false>(a, st);
-    return alibi ? launch_dq_t<64, false, true>(a, st) : launch_dq_t<64, false, false>(a, st);
-  }
-  if (a.bf16) return alibi ? launch_dq_t<128, true, true>(a, st) : launch_dq_t<128, true, false>(a, st);
-  return alibi ? launch_dq_t<128, false, true>(a, st) : launch_dq_t<128, false, false>(a, st);
+  if (a.D == 64) return a.bf16 ? launch_dq_d<64, true>(a, st) : launch_dq_d<64, false>(a, st);
+  return a.bf16 ? launch_dq_d<128, true>(a, st) : launch_dq_d<128, false>(a, st);
 }
 
 cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N, int H,

@@ -53,7 +53,7 @@ constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+template <int D, bool kSparse>
 struct FwdSmem {
   static constexpr int kBlocks = D / 64;             // 64-element column blocks
   static constexpr int kBlockBytes = kTile * 128;    // 128 rows x 128 B
@@ -67,6 +67,37 @@ struct FwdSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  // block-sparse: key tiles of tile A, of tile B, and their union
+  uint32_t key_tiles[kSparse ? 3 : 1][kSparse ? kMaxSparseTiles / 32 : 1];
+};
+
+// The key tiles one CTA multiplies: for each query tile t a range
+// [lo_t, hi_t] (dense) or a set (block-sparse), and the K/V stream over
+// their union in increasing order.  Every walk ends at the sentinel n.
+template <bool kSparse>
+struct KeyWalk {
+  int lo0, hi0, lo1, hi1, last, n;
+  TileSet a, b, u;
+  __device__ __forceinline__ int first() const { return kSparse ? u.next(0) : lo0; }
+  __device__ __forceinline__ int next(int j) const {
+    return kSparse ? u.next(j + 1) : (j + 1 <= last ? j + 1 : n);
+  }
+  __device__ __forceinline__ bool has(int t, int j) const {
+    if (kSparse) return t ? b.has(j) : a.has(j);
+    return t ? (j >= lo1 && j <= hi1) : (j >= lo0 && j <= hi0);
+  }
+  __device__ __forceinline__ int first_of(int t) const {
+    if (kSparse) return t ? b.next(0) : a.next(0);
+    return t ? (lo1 <= hi1 ? lo1 : n) : (lo0 <= hi0 ? lo0 : n);
+  }
+  __device__ __forceinline__ int next_of(int t, int j) const {
+    if (kSparse) return t ? b.next(j + 1) : a.next(j + 1);
+    return j + 1 <= (t ? hi1 : hi0) ? j + 1 : n;
+  }
+  __device__ __forceinline__ int count_of(int t) const {
+    if (kSparse) return t ? b.count() : a.count();
+    return t ? max(0, hi1 - lo1 + 1) : max(0, hi0 - lo0 + 1);
+  }
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
@@ -75,9 +106,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool kBf16, bool kAlibi>
+template <int D, bool kBf16, bool kAlibi, bool kSparse>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
-  using Smem = FwdSmem<D>;
+  using Smem = FwdSmem<D, kSparse>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -108,8 +139,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       band_key_tiles(qt * kTile, kTile, kTile, n_kv, wl, wr, lo[t], hi[t]);
     }
   }
-  const int j_first = lo[0], j_last = max(hi[0], hi[1]);
   const int n_q_here = hi[1] >= lo[1] ? 2 : 1;
+  KeyWalk<kSparse> walk{lo[0], hi[0], lo[1], hi[1], max(hi[0], hi[1]), n_kv,
+                        TileSet{s.key_tiles[0], n_kv},
+                        TileSet{s.key_tiles[kSparse ? 1 : 0], n_kv},
+                        TileSet{s.key_tiles[kSparse ? 2 : 0], n_kv}};
+  if constexpr (kSparse) {
+    // the block mask, intersected with each tile's band range
+    const int qa = 2 * pt, qb = 2 * pt + 1;
+    auto in_a = [&](int j) {
+      return j >= lo[0] && j <= hi[0] && block_kept(p.band, bh, p.H, n_kv, qa, j);
+    };
+    auto in_b = [&](int j) {
+      return j >= lo[1] && j <= hi[1] && block_kept(p.band, bh, p.H, n_kv, qb, j);
+    };
+    fill_tile_set(s.key_tiles[0], n_kv, in_a);
+    fill_tile_set(s.key_tiles[1], n_kv, in_b);
+    fill_tile_set(s.key_tiles[2], n_kv, [&](int j) { return in_a(j) || in_b(j); });
+  }
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
@@ -147,9 +194,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full, kb * 64,
                       (2 * pt + t) * kTile, hh, bb);
       int issued = 0;
-      for (int j = j_first; j <= j_last; ++j) {
-        const int jj = j - j_first;  // position in the stream
-        const int st = jj & 1;
+      for (int j = walk.first(), jj = 0; j < walk.n; j = walk.next(j), ++jj) {
+        const int st = jj & 1;  // jj: position in the stream
         const uint32_t u = static_cast<uint32_t>(jj >> 1);
         if (jj >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
@@ -187,10 +233,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       const uint64_t dq0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(s.v[0]), Smem::kBlockBytes, 1024);
-      // S_t(j) = Q_t K_j^T into tile t's S columns
-      auto issue_s = [&](int t, int j) {
+      // S_t = Q_t K^T into tile t's S columns, K from stage kst
+      auto issue_s = [&](int t, int kst) {
         const uint64_t dq = desc_add(dq0, t * Smem::kTileBytes);
-        const uint64_t dk = desc_add(dk0, ((j - j_first) & 1) * Smem::kTileBytes);
+        const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
@@ -199,53 +245,107 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
         tc_commit(&s.s_full[t]);
       };
+      const int jf = walk.first();
+      // with nothing to multiply (an empty block-sparse pair) no K arrives
       bool ok = mbar_wait(&s.q_full, 0, p.err, abort_flag) &&
-                mbar_wait(&s.k_full[0], 0, p.err, abort_flag);
-      if (ok) {
+                (jf >= walk.n || mbar_wait(&s.k_full[0], 0, p.err, abort_flag));
+      if (ok && jf < walk.n) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (lo[t] == j_first && lo[t] <= hi[t]) issue_s(t, j_first);
+          if (walk.has(t, jf)) issue_s(t, 0);
         tc_commit(&s.k_empty[0]);
       }
-      for (int j = j_first; ok && j <= j_last; ++j) {
-        const int jj = j - j_first;
-        const int st = jj & 1;
-        if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
-        bool k_next = false;  // K_{j+1} has landed
-        for (int t = 0; ok && t < 2; ++t) {
-          const int lt = t ? lo[1] : lo[0], ht = t ? hi[1] : hi[0];
-          const bool active = j >= lt && j <= ht;
-          // S_t(j+1) is next: after PV_t(j), or as the first product of a
-          // tile whose range starts at j + 1
-          const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
-          if (active) {
-            if (!mbar_wait(&s.p_full[t], (j - lt) & 1, p.err, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // O_t += P_t(j) V_j, with P read from tile t's S columns
-            const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
-                        desc_add(dv, kk * 16 * 128), idPV, (j > lt || kk > 0) ? 1u : 0u);
-            tc_commit(&s.o_done[t]);
-          }
-          if (s_next) {
-            if (!k_next) {
-              if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err, abort_flag)) {
+      if constexpr (!kSparse) {
+        // dense: each tile's key tiles are the range [lo_t, hi_t]
+        const int j_first = jf, j_last = walk.last;
+        for (int j = j_first; ok && j <= j_last; ++j) {
+          const int jj = j - j_first;
+          const int st = jj & 1;
+          if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
+          bool k_next = false;  // K_{j+1} has landed
+          for (int t = 0; ok && t < 2; ++t) {
+            const int lt = t ? lo[1] : lo[0], ht = t ? hi[1] : hi[0];
+            const bool active = j >= lt && j <= ht;
+            // S_t(j+1) is next: after PV_t(j), or as the first product of a
+            // tile whose range starts at j + 1
+            const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
+            if (active) {
+              if (!mbar_wait(&s.p_full[t], (j - lt) & 1, p.err, abort_flag)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              k_next = true;
+              // O_t += P_t(j) V_j, with P read from tile t's S columns
+              const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
+                          desc_add(dv, kk * 16 * 128), idPV, (j > lt || kk > 0) ? 1u : 0u);
+              tc_commit(&s.o_done[t]);
             }
-            issue_s(t, j + 1);  // after the PV product that read P_t(j)
+            if (s_next) {
+              if (!k_next) {
+                if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err,
+                               abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_next = true;
+              }
+              issue_s(t, (jj + 1) & 1);  // after the PV product that read P_t(j)
+            }
           }
+          tc_commit(&s.v_empty[st]);
+          if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
         }
-        tc_commit(&s.v_empty[st]);
-        if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
+      } else {
+        // block-sparse: each tile's key tiles are a set; counters give the
+        // p_full phases
+        int c0 = 0, c1 = 0;  // P V products issued for tile A, B (p_full phases)
+        for (int j = jf, jj = 0, jn = 0; ok && j < walk.n; j = jn, ++jj) {
+          jn = walk.next(j);  // the stream's next key tile
+          const int st = jj & 1;
+          if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
+          bool k_next = false;  // K of tile jn has landed
+          for (int t = 0; ok && t < 2; ++t) {
+            const bool active = walk.has(t, j);
+            // S_t of tile jn follows PV_t(j), or starts a tile that joins at jn
+            const bool s_next = jn < walk.n && walk.has(t, jn);
+            if (active) {
+              const int ct = t ? c1 : c0;
+              if (!mbar_wait(&s.p_full[t], ct & 1, p.err, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // O_t += P_t(j) V_j, with P read from tile t's S columns
+              const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+  #pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
+                          desc_add(dv, kk * 16 * 128), idPV, (ct > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(&s.o_done[t]);
+              if (t)
+                ++c1;
+              else
+                ++c0;
+            }
+            if (s_next) {
+              if (!k_next) {
+                if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_next = true;
+              }
+              issue_s(t, (jj + 1) & 1);  // after the PV product that read P_t(j)
+            }
+          }
+          tc_commit(&s.v_empty[st]);
+          if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
+        }
       }
       // Every MMA issued above completes before TMEM is released.
       tc_commit(&s.drain);
@@ -258,8 +358,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const int r = tid & 127;          // row within the tile and TMEM lane
     const int q0 = (2 * pt + t) * kTile;
     const int i = q0 + r;
-    const int t_lo = t ? lo[1] : lo[0];
-    const int n_tiles = max(0, (t ? hi[1] : hi[0]) - t_lo + 1);
+    const int n_tiles = walk.count_of(t);
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + t * 128, tO = tbase + 256 + t * D;
@@ -268,8 +367,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     float m = -INFINITY;  // reference maximum, log2 units
     float l = 0.f;        // running sum of 2^(t - m)
     bool ok = true;
-    for (int jj = 0; jj < n_tiles; ++jj) {
-      const int j = t_lo + jj;
+    for (int jj = 0, j = walk.first_of(t); jj < n_tiles; ++jj, j = walk.next_of(t, j)) {
       if (!warp_wait(&s.s_full[t], jj & 1, p.err, abort_flag)) {
         ok = false;
         break;
@@ -379,8 +477,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     // ---------------------------------------------------------- epilogue
     // Every thread of the group takes the same branch (a timeout in one warp
     // must not leave the others waiting at the barrier below).
-    if (n_tiles > 0) {
-      const bool mine = ok && warp_wait(&s.o_done[t], (n_tiles - 1) & 1, p.err, abort_flag);
+    if (q0 < p.N) {
+      // A tile the block mask empties has O = 0 and LSE = -inf; its smem
+      // stage may be written once its Q load has landed.
+      const bool have = n_tiles > 0;
+      const bool mine =
+          ok && (have ? warp_wait(&s.o_done[t], (n_tiles - 1) & 1, p.err, abort_flag)
+                      : warp_wait(&s.q_full, 0, p.err, abort_flag));
       if (named_bar_and(1 + t, 128, mine)) {
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -388,8 +491,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(tO + lane_off + c * 32, o);
-          tmem_ld_wait();
+          if (have) {
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -412,7 +520,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           tma_store_commit();
           tma_store_wait_all();
         }
-        if (i < p.N) p.lse[static_cast<long long>(bh) * p.N + i] = (m + lg2_approx(l)) * kLn2;
+        if (i < p.N)
+          p.lse[static_cast<long long>(bh) * p.N + i] =
+              have ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -425,10 +535,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   }
 }
 
-template <int D, bool kBf16, bool kAlibi>
+template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, kBf16, kAlibi>;
-  const int smem = static_cast<int>(sizeof(FwdSmem<D>)) + 1024;
+  auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse>;
+  const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse>)) + 1024;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -444,14 +554,17 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 
 }  // namespace
 
+template <int D, bool kBf16>
+cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
+  const bool alibi = a.band.alibi != nullptr, sparse = a.band.block_mask != nullptr;
+  if (sparse)
+    return alibi ? launch_fwd_t<D, kBf16, true, true>(a, s) : launch_fwd_t<D, kBf16, false, true>(a, s);
+  return alibi ? launch_fwd_t<D, kBf16, true, false>(a, s) : launch_fwd_t<D, kBf16, false, false>(a, s);
+}
+
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {
-  const bool alibi = a.band.alibi != nullptr;
-  if (a.D == 64) {
-    if (a.bf16) return alibi ? launch_fwd_t<64, true, true>(a, s) : launch_fwd_t<64, true, false>(a, s);
-    return alibi ? launch_fwd_t<64, false, true>(a, s) : launch_fwd_t<64, false, false>(a, s);
-  }
-  if (a.bf16) return alibi ? launch_fwd_t<128, true, true>(a, s) : launch_fwd_t<128, true, false>(a, s);
-  return alibi ? launch_fwd_t<128, false, true>(a, s) : launch_fwd_t<128, false, false>(a, s);
+  if (a.D == 64) return a.bf16 ? launch_fwd_d<64, true>(a, s) : launch_fwd_d<64, false>(a, s);
+  return a.bf16 ? launch_fwd_d<128, true>(a, s) : launch_fwd_d<128, false>(a, s);
 }
 
 }  // namespace fa

@@ -17,11 +17,20 @@ constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 // a negative bound being absent; the causal mask is win_right = 0.  ALiBi:
 // the score of (i, j) gets -slope * |i - j| added, slope =
 // alibi[(bh / H) * alibi_bstride + bh % H] (alibi == nullptr: no bias).
+// Block-sparse: query tile qt multiplies key tile kt (tiles of kTile rows)
+// only when block_mask[(bh % H) * bm_head_stride + qt * n_kt + kt] != 0
+// (block_mask == nullptr: every tile pair).
 struct Band {
   int win_left, win_right;
   const float* alibi;
   int alibi_bstride;
+  const uint8_t* block_mask;
+  long long bm_head_stride;
 };
+
+// Largest number of tiles along N a block-sparse call may have (the tile
+// sets live in shared memory as bitmasks).
+constexpr int kMaxSparseTiles = 16384;
 
 struct FwdLaunch {
   CUtensorMap map_q, map_k, map_v, map_o;  // box 64 x 128 x 1 x 1, 128B swizzle

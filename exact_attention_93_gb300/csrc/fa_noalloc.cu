@@ -103,7 +103,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   a.H = H;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.band = Band{-1, causal ? 0 : -1, nullptr, 0};
+  a.band = Band{-1, causal ? 0 : -1, nullptr, 0, nullptr, 0};
   a.bf16 = dtype == FA_BF16 ? 1 : 0;
   a.err = err;
 

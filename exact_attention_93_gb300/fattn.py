@@ -36,9 +36,10 @@ class FaLayout(ctypes.Structure):
 
 
 class FaOptions(ctypes.Structure):
-    """fa_options: sliding window (-1 = no bound) and ALiBi slopes."""
+    """fa_options: sliding window (-1 = no bound), ALiBi slopes, block mask."""
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
-                ("alibi_slopes", ctypes.c_void_p), ("alibi_per_batch", ctypes.c_int)]
+                ("alibi_slopes", ctypes.c_void_p), ("alibi_per_batch", ctypes.c_int),
+                ("block_mask", ctypes.c_void_p), ("block_mask_per_head", ctypes.c_int)]
 
 
 class FattnError(RuntimeError):
@@ -201,10 +202,22 @@ def fa_bwd_strided(q, k, v, o, lse, do, dq, dk, dv, layout: FaLayout, B: int, H:
     _check(st, "fa_bwd_strided")
 
 
-def options(window=(-1, -1), alibi_slopes=None) -> FaOptions:
-    """fa_options for a window (left, right) and optional fp32 CUDA slopes of
-    shape [H] or [B, H] (kept alive by the caller until the call is done)."""
-    opt = FaOptions(int(window[0]), int(window[1]), None, 0)
+def options(window=(-1, -1), alibi_slopes=None, block_mask=None) -> FaOptions:
+    """fa_options for a window (left, right), optional fp32 CUDA slopes of
+    shape [H] or [B, H], and an optional uint8 CUDA block mask of shape
+    [T, T] or [H, T, T], T = ceil(N / 128).  The returned object keeps the
+    tensors it points at alive; the kernels read them when they run, so the
+    caller keeps it (or the tensors) until the stream has passed the call."""
+    opt = FaOptions(int(window[0]), int(window[1]), None, 0, None, 0)
+    opt._tensors = (alibi_slopes, block_mask)
+    if block_mask is not None:
+        torch = _torch()
+        if block_mask.dtype not in (torch.uint8, torch.bool) or not block_mask.is_cuda:
+            raise ValueError("block_mask must be a uint8 or bool CUDA tensor")
+        if not block_mask.is_contiguous() or block_mask.dim() not in (2, 3):
+            raise ValueError("block_mask must be a contiguous [T, T] or [H, T, T] tensor")
+        opt.block_mask = block_mask.data_ptr()
+        opt.block_mask_per_head = 1 if block_mask.dim() == 3 else 0
     if alibi_slopes is not None:
         torch = _torch()
         if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda:

@@ -104,11 +104,24 @@ typedef struct {
  *                              -slope * |i - j| added after scaling.
  *                              4-byte aligned; read by the kernels, not
  *                              validated.
+ *   block_mask                 NULL, or a device array of bytes over blocks
+ *                              of 128 x 128 scores, [T][T] for every head
+ *                              (block_mask_per_head = 0) or [H][T][T] (= 1),
+ *                              T = ceil(N / 128): query block a multiplies
+ *                              key block b only when the byte [a][b] is
+ *                              nonzero (block-sparse attention, the
+ *                              extension [DEEP] and [WALK] report).  It
+ *                              combines with causal, the window and ALiBi;
+ *                              a row left with no visible key gets O = 0,
+ *                              LSE = -inf and no gradient.  T may be at most
+ *                              16384 (FA_ERR_UNSUPPORTED beyond).
  */
 typedef struct {
   int window_left, window_right;
   const float* alibi_slopes;
   int alibi_per_batch;
+  const unsigned char* block_mask;
+  int block_mask_per_head;
 } fa_options;
 
 /*

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 3
+    assert lib.fa_abi_version() == 4
     names = [lib.fa_status_string(i).decode() for i in range(5)]
     assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
                      "FA_ERR_TIMEOUT"]
@@ -182,7 +182,7 @@ def test_strides_of_reads_named_dimensions():
 
 @pytest.mark.parametrize("win", [(-2, 0), (0, -2), (-5, -5)])
 def test_ex_entry_points_reject_bad_windows(lib, win):
-    opt = fattn.FaOptions(win[0], win[1], None, 0)
+    opt = fattn.FaOptions(win[0], win[1], None, 0, None, 0)
     assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 128, 64, None, ctypes.byref(opt),
                          ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_INVALID_ARG
     need = lib.fa_bwd_workspace_size(1, 2, 128, 64, 0)
@@ -192,6 +192,13 @@ def test_ex_entry_points_reject_bad_windows(lib, win):
 
 
 def test_ex_entry_points_reject_misaligned_slopes(lib):
-    opt = fattn.FaOptions(-1, -1, FAKE + 2, 0)
+    opt = fattn.FaOptions(-1, -1, FAKE + 2, 0, None, 0)
     assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 128, 64, None, ctypes.byref(opt),
                          ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_INVALID_ARG
+
+
+def test_block_mask_beyond_the_tile_limit_is_unsupported(lib):
+    opt = fattn.FaOptions(-1, -1, None, 0, FAKE, 0)
+    N = 128 * 16384 + 1                      # 16385 tiles along N
+    assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, N, 64, None, ctypes.byref(opt),
+                         ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_UNSUPPORTED

@@ -34,3 +34,8 @@ def test_packed_shape_is_checked():
 def test_cpu_tensors_are_refused():
     with pytest.raises(ValueError):
         flash_attn_func(x(), x(), x())
+
+
+def test_block_mask_shape_is_checked():
+    with pytest.raises(ValueError):
+        flash_attn_func(x(), x(), x(), block_mask=torch.ones(2, 2, dtype=torch.uint8))
