@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 // shared memory, which bounds them at 48 cycles per 128 x 64 x 16 product.
 // dQ is formed transposed, dQ^T = K^T dS^T (M = D), so TMEM lane = column d
 // and each atomic warp instruction covers 32 consecutive floats of one dQ row.
-constexpr int kD128Threads = 480;  // warps 0-7 elementwise, 8-11 dQ, 12 producer, 13-14 MMA
+constexpr int kD128Threads = 480;  // warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA
 constexpr int kQ64 = 64;
 
 template <bool kSparse>
@@ -455,7 +455,8 @@ struct Dkdv128Smem {
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
-  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], p_full[2], kv_done[2];
+  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], s_read[2], p_full[2], kv_done[2];
+  uint64_t buf_ready[2];
   uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -501,6 +502,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
+      mbar_init(&s.s_read[i], 8);  // one arrival per elementwise warp
+      mbar_init(&s.buf_ready[i], 4);  // one arrival per buffer warp
       mbar_init(&s.kv_done[i], 1);
       mbar_init(&s.tmem_free[i], 128);
       mbar_init(&s.drain[i], 1);
@@ -560,13 +563,17 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
-        // Buffer b last held tile it - 2, whose P^T / dS^T feed dV, dK(it - 2),
-        // and dQ^T(it - 3), which the dQ warps drain.
-        if (it >= 2 && !mbar_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) break;
-        if (kAtomicDq && it >= 3 &&
-            !mbar_wait(&s.tmem_free[b], ((it - 3) >> 1) & 1, p.err, abort_flag))
-          break;
-        if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
+        if (kAtomicDq) {
+          // The buffer warps signal when buffer b may take tile it: one wait
+          // here instead of three (each wait of this thread costs tensor
+          // time).
+          if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        } else {
+          // Without dQ^T only dV, dK(it - 2) and the Q / dO load gate the
+          // buffer; a relay through the buffer warps would only add latency.
+          if (it >= 2 && !mbar_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) break;
+          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
+        }
         tc_fence_after();
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
 #pragma unroll
@@ -609,6 +616,20 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       };
       for (int it = 0; it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
+        if (kAtomicDq && it >= 1) {
+          // S^T(it) is in the elementwise warps' registers: dQ^T(it - 1) can
+          // take its columns (their previous occupant, dQ^T(it - 3), was
+          // drained before S^T(it) was issued), and dS^T(it - 1) reached
+          // shared memory before that signal.  It runs while the
+          // elementwise step of tile it does, off the chain that frees
+          // buffer b for S^T(it + 2).
+          if (!mbar_wait(&s.s_read[b], (it >> 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_dq(it - 1);
+        }
         if (!mbar_wait(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) {
           ok = false;
           break;
@@ -629,12 +650,6 @@ __global__ void __launch_bounds__(kD128Threads, 1)
                     (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&s.qdo_empty[st]);
         tc_commit(&s.kv_done[b]);
-        // S^T(it) is consumed: dQ^T(it - 1) can take its columns (their
-        // previous occupant, dQ^T(it - 3), was drained before S^T(it) was
-        // issued).  dS^T(it - 1) reached shared memory before P(it) was
-        // signalled.  dQ^T goes after dV, dK so that buffer b is released
-        // to the score warp as early as possible.
-        if (kAtomicDq && it >= 1) issue_dq(it - 1);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it and the last dS^T is in shared memory.
@@ -655,22 +670,40 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ drain
-    if (kAtomicDq) {
-      const int quad = warp & 3;
-      const int d = quad * 32 + lane;  // TMEM lane = column d of dQ
-      const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-      for (int j = 0, qt = walk.first(); j < n_it; ++j, qt = walk.next(qt)) {
+    // ------------------------------------------------------------ buffer warps
+    // Atomic mode: buffer it & 1 may take S^T, dP^T(it) once dV, dK(it - 2)
+    // are done (the last readers of its P^T / dS^T), dQ^T(it - 3) has left
+    // its S^T columns and Q / dO(it) have landed.  These warps wait for all
+    // three, signal buf_ready(it), and drain dQ^T (TMEM lane = column d of
+    // dQ) into the fp32 accumulator.
+    const int quad = warp & 3;
+    const int d = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    int qt_dq = walk.first();  // query tile of the dQ^T drained next
+    for (int it = 0; kAtomicDq && it < n_it + 3; ++it) {
+      const int b = it & 1;
+      const int j = it - 3;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) & 1 = b
+      const bool drain = j >= 0 && j < n_it;
+      uint32_t g[2][32];
+      if (drain) {
         if (!warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag)) break;
         tc_fence_after();
-        const int b = (j + 1) & 1;  // dQ^T(j) sits in the S^T columns of tile j + 1
-        uint32_t g[2][32];
         tmem_ld32(tbase + lane_off + b * 128, g[0]);
         tmem_ld32(tbase + lane_off + b * 128 + 32, g[1]);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&s.tmem_free[b]);
-        const int q0 = qt * kQ64;
+        mbar_arrive(&s.tmem_free[b]);  // for the last tile's dQ^T
+      }
+      if (it < n_it) {
+        if ((it >= 2 && !warp_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) ||
+            !warp_wait(&s.qdo_full[it % 3], (it / 3) & 1, p.err, abort_flag))
+          break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.buf_ready[b]);
+      }
+      if (drain) {
+        const int q0 = qt_dq * kQ64;
+        qt_dq = walk.next(qt_dq);
         float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
         const int nq = min(kQ64, p.N - q0);
 #pragma unroll
@@ -704,6 +737,13 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
       tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
       tmem_ld_wait();
+      if (kAtomicDq) {
+        // S^T(it) has left TMEM (and dS^T(it - 1), stored in the previous
+        // iteration, is in shared memory): dQ^T(it - 1) may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.s_read[b]);
+      }
       const bool cut = band_cuts(q0, kQ64, k0, kTile, wl, wr);
       uint32_t pk[16], dk[16];
       if (!cut && !kAlibi) {
