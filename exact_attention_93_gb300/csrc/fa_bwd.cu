@@ -503,7 +503,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
       mbar_init(&s.s_read[i], 8);  // one arrival per elementwise warp
-      mbar_init(&s.buf_ready[i], 4);  // one arrival per buffer warp
+      // four buffer warps and the tcgen05.commit that retires dV, dK(it - 2)
+      mbar_init(&s.buf_ready[i], 5);
       mbar_init(&s.kv_done[i], 1);
       mbar_init(&s.tmem_free[i], 128);
       mbar_init(&s.drain[i], 1);
@@ -649,7 +650,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
                     desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                     (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&s.qdo_empty[st]);
-        tc_commit(&s.kv_done[b]);
+        // dV, dK(it) done frees buffer b for tile it + 2: in atomic mode the
+        // commit arrives on buf_ready(it + 2) itself, so the score warp wakes
+        // on the tensor core's arrival, not on a relay.
+        tc_commit(kAtomicDq ? &s.buf_ready[b] : &s.kv_done[b]);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it and the last dS^T is in shared memory.
@@ -672,10 +676,11 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------------------ buffer warps
     // Atomic mode: buffer it & 1 may take S^T, dP^T(it) once dV, dK(it - 2)
-    // are done (the last readers of its P^T / dS^T), dQ^T(it - 3) has left
-    // its S^T columns and Q / dO(it) have landed.  These warps wait for all
-    // three, signal buf_ready(it), and drain dQ^T (TMEM lane = column d of
-    // dQ) into the fp32 accumulator.
+    // are done (the last readers of its P^T / dS^T; their tcgen05.commit
+    // arrives on buf_ready(it) directly), dQ^T(it - 3) has left its S^T
+    // columns and Q / dO(it) have landed.  These warps see to the last two,
+    // arrive on buf_ready(it), and drain dQ^T (TMEM lane = column d of dQ)
+    // into the fp32 accumulator.
     const int quad = warp & 3;
     const int d = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -695,11 +700,13 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         mbar_arrive(&s.tmem_free[b]);  // for the last tile's dQ^T
       }
       if (it < n_it) {
-        if ((it >= 2 && !warp_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) ||
-            !warp_wait(&s.qdo_full[it % 3], (it / 3) & 1, p.err, abort_flag))
-          break;
+        if (!warp_wait(&s.qdo_full[it % 3], (it / 3) & 1, p.err, abort_flag)) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.buf_ready[b]);
+        if (lane == 0) {
+          mbar_arrive(&s.buf_ready[b]);
+          // tiles 0 and 1 have no dV, dK(it - 2) to wait for
+          if (it < 2 && warp == 8) mbar_arrive(&s.buf_ready[b]);
+        }
       }
       if (drain) {
         const int q0 = qt_dq * kQ64;
