@@ -455,7 +455,7 @@ struct Dkdv128Smem {
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
-  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], s_read[2], p_full[2], kv_done[2];
+  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], s_read[2], p_full[2];
   uint64_t buf_ready[2];
   uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
   uint32_t tmem_base;
@@ -505,7 +505,6 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       mbar_init(&s.s_read[i], 8);  // one arrival per elementwise warp
       // four buffer warps and the tcgen05.commit that retires dV, dK(it - 2)
       mbar_init(&s.buf_ready[i], 5);
-      mbar_init(&s.kv_done[i], 1);
       mbar_init(&s.tmem_free[i], 128);
       mbar_init(&s.drain[i], 1);
     }
@@ -564,17 +563,9 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
-        if (kAtomicDq) {
-          // The buffer warps signal when buffer b may take tile it: one wait
-          // here instead of three (each wait of this thread costs tensor
-          // time).
-          if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
-        } else {
-          // Without dQ^T only dV, dK(it - 2) and the Q / dO load gate the
-          // buffer; a relay through the buffer warps would only add latency.
-          if (it >= 2 && !mbar_wait(&s.kv_done[b], ((it - 2) >> 1) & 1, p.err, abort_flag)) break;
-          if (!mbar_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) break;
-        }
+        // Buffer b may take tile it once buf_ready(it) completes: one wait
+        // here instead of three (each wait of this thread costs tensor time).
+        if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
 #pragma unroll
@@ -650,10 +641,10 @@ __global__ void __launch_bounds__(kD128Threads, 1)
                     desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                     (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&s.qdo_empty[st]);
-        // dV, dK(it) done frees buffer b for tile it + 2: in atomic mode the
-        // commit arrives on buf_ready(it + 2) itself, so the score warp wakes
-        // on the tensor core's arrival, not on a relay.
-        tc_commit(kAtomicDq ? &s.buf_ready[b] : &s.kv_done[b]);
+        // dV, dK(it) done frees buffer b for tile it + 2: the commit arrives
+        // on buf_ready(it + 2) itself, so the score warp wakes on the tensor
+        // core's arrival, not on a relay.
+        tc_commit(&s.buf_ready[b]);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it and the last dS^T is in shared memory.
@@ -675,20 +666,20 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ buffer warps
-    // Atomic mode: buffer it & 1 may take S^T, dP^T(it) once dV, dK(it - 2)
-    // are done (the last readers of its P^T / dS^T; their tcgen05.commit
-    // arrives on buf_ready(it) directly), dQ^T(it - 3) has left its S^T
-    // columns and Q / dO(it) have landed.  These warps see to the last two,
-    // arrive on buf_ready(it), and drain dQ^T (TMEM lane = column d of dQ)
-    // into the fp32 accumulator.
+    // Buffer it & 1 may take S^T, dP^T(it) once dV, dK(it - 2) are done (the
+    // last readers of its P^T / dS^T; their tcgen05.commit arrives on
+    // buf_ready(it) directly), dQ^T(it - 3) has left its S^T columns (atomic
+    // mode) and Q / dO(it) have landed.  These warps see to the last two,
+    // arrive on buf_ready(it), and in atomic mode drain dQ^T (TMEM lane =
+    // column d of dQ) into the fp32 accumulator.
     const int quad = warp & 3;
     const int d = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     int qt_dq = walk.first();  // query tile of the dQ^T drained next
-    for (int it = 0; kAtomicDq && it < n_it + 3; ++it) {
+    for (int it = 0; it < n_it + (kAtomicDq ? 3 : 0); ++it) {
       const int b = it & 1;
       const int j = it - 3;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) & 1 = b
-      const bool drain = j >= 0 && j < n_it;
+      const bool drain = kAtomicDq && j >= 0 && j < n_it;
       uint32_t g[2][32];
       if (drain) {
         if (!warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag)) break;
