@@ -12,7 +12,10 @@ sliding-window local attention (query i sees keys i - left .. i + right,
 -slope * |i - j| to each score, as the page documents.  block_mask (an
 extension of that argument list) restricts attention to the kept blocks of
 128 x 128 scores: block-sparse attention.  Dropout is not provided; asking
-for it raises.
+for it raises.  flash_attn_fp8_func is the forward on e4m3 inputs
+(FlashAttention-3's FP8 forward, which the "Flash Attention" wiki page and
+the v1 -> v3 table of "FlashAttention 深入" list), with per-(batch, head)
+descale factors; it has no backward.
 """
 from __future__ import annotations
 
@@ -20,7 +23,7 @@ import torch
 
 from . import fattn
 
-__all__ = ["flash_attn_func", "flash_attn_qkvpacked_func"]
+__all__ = ["flash_attn_func", "flash_attn_qkvpacked_func", "flash_attn_fp8_func"]
 
 
 def _check_block_mask(block_mask, N, H):
@@ -158,4 +161,30 @@ def flash_attn_qkvpacked_func(qkv, dropout_p=0.0, softmax_scale=None, causal=Fal
     scale = qkv.shape[-1] ** -0.5 if softmax_scale is None else float(softmax_scale)
     o, lse = _FlashAttnQKVPacked.apply(qkv, scale, bool(causal), window, slopes, bmask,
                                        bool(deterministic))
+    return (o, lse) if return_lse else o
+
+
+def flash_attn_fp8_func(q, k, v, softmax_scale=None, causal=False, window_size=(-1, -1),
+                        alibi_slopes=None, block_mask=None, descale_q=None, descale_k=None,
+                        descale_v=None, return_lse=False):
+    """Forward-only attention of e4m3 q, k, v (torch.float8_e4m3fn, shaped
+    (batch, seqlen, nheads, 128), head dim contiguous, other strides multiples
+    of 16).  descale_q / descale_k / descale_v: None or fp32 (batch, nheads)
+    factors; the result is attention of descale_q * q, descale_k * k and
+    descale_v * v, returned in bf16 (with the fp32 (batch, nheads, seqlen)
+    log-sum-exp when return_lse).  window_size, alibi_slopes and block_mask
+    as for flash_attn_func."""
+    B, N, H, D = (int(x) for x in q.shape)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same (batch, seqlen, nheads, headdim) shape")
+    window, slopes = _check_options(0.0, window_size, alibi_slopes, B, H)
+    bmask = _check_block_mask(block_mask, N, H)
+    desc = [None if t is None else t.to(torch.float32).reshape(B, H).contiguous()
+            for t in (descale_q, descale_k, descale_v)]
+    scale = D ** -0.5 if softmax_scale is None else float(softmax_scale)
+    o = torch.empty((B, N, H, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    opts = fattn.options(window, slopes, bmask)
+    fattn.fa_fwd_fp8(q, k, v, o, lse, _layout(q, k, v, o), opts, B, H, N, D, scale,
+                     bool(causal), *desc)
     return (o, lse) if return_lse else o

@@ -174,7 +174,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 4; }
+int fa_abi_version(void) { return 5; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -218,6 +218,76 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   a.err = error_word_ptr();
   if (!a.err) return FA_ERR_CUDA;
   return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+// 8-bit operands: strides in bytes, multiples of 16.
+fa_status check_strides_u8(const Shape& s, const RowStrides& r) {
+  const long long st[3] = {r.batch, r.head, r.seq};
+  for (long long x : st)
+    if (x < 0 || (x & 15) != 0) return FA_ERR_INVALID_ARG;
+  const double last = static_cast<double>(s.B - 1) * r.batch + static_cast<double>(s.H - 1) * r.head +
+                      static_cast<double>(s.N - 1) * r.seq + s.D;
+  return last < 1099511627776.0 ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+// Row pitch of the V^T scratch: N rounded up to 16 bytes.
+long long vt_pitch(const Shape& s) { return (static_cast<long long>(s.N) + 15) / 16 * 16; }
+
+size_t fwd8_ws_bytes(const Shape& s) {
+  return round256(static_cast<size_t>(s.BH()) * s.D * static_cast<size_t>(vt_pitch(s)));
+}
+
+bool aligned4_or_null(const float* p) { return !p || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+fa_status fwd8_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const Shape& s, const Layout& L, const fa_options* opt,
+                    const float* descale_q, const float* descale_k, const float* descale_v,
+                    float scale, int causal, void* ws, size_t ws_bytes, void* stream) {
+  fa_status st = check_shape(s, FA_BF16);
+  if (st != FA_OK) return st;
+  if (s.D != 128) return FA_ERR_UNSUPPORTED;
+  Band band;
+  if ((st = make_band(opt, causal, s, &band)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned4_or_null(descale_q) || !aligned4_or_null(descale_k) ||
+      !aligned4_or_null(descale_v))
+    return FA_ERR_INVALID_ARG;
+  for (const RowStrides* r : {&L.q, &L.k, &L.v})
+    if ((st = check_strides_u8(s, *r)) != FA_OK) return st;
+  if ((st = check_strides(s, L.o)) != FA_OK) return st;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < fwd8_ws_bytes(s))
+    return FA_ERR_INVALID_ARG;
+  const long long ld = vt_pitch(s);
+  FwdLaunch a{};
+  if (!operand_map_u8(&a.map_q, q, s.B, s.H, s.N, s.D, L.q.batch, L.q.head, L.q.seq, kTile) ||
+      !operand_map_u8(&a.map_k, k, s.B, s.H, s.N, s.D, L.k.batch, L.k.head, L.k.seq, kTile) ||
+      !make_tmap_4d(&a.map_v, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(s.N),
+                    static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.H),
+                    static_cast<uint64_t>(s.B), static_cast<uint64_t>(ld),
+                    static_cast<uint64_t>(ld) * s.D, static_cast<uint64_t>(ld) * s.D * s.H, 128,
+                    static_cast<uint32_t>(s.D), CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+      !tile_map(&a.map_o, o, s, FA_BF16, L.o))
+    return FA_ERR_CUDA;
+  a.lse = lse;
+  a.N = s.N;
+  a.BH = static_cast<int>(s.BH());
+  a.D = s.D;
+  a.H = s.H;
+  a.scale_log2 = scale * kLog2e;
+  a.band = band;
+  a.bf16 = 1;
+  a.fp8 = 1;
+  a.descale_q = descale_q;
+  a.descale_k = descale_k;
+  a.descale_v = descale_v;
+  a.err = error_word_ptr();
+  if (!a.err) return FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_transpose_v8(v, L.v, ws, s.N, ld, s.H, s.BH(), s.D, cs);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  return from_cuda(launch_fwd(a, cs));
 }
 
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -279,6 +349,23 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   const Shape s{B, H, N, D};
   return fwd_impl(q, k, v, o, lse, s, layout ? from_abi(*layout) : contiguous_layout(s), scale,
                   causal, options, dtype, stream);
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int D) {
+  const Shape s{B, H, N, D};
+  if (check_shape(s, FA_BF16) != FA_OK || D != 128) return 0;
+  return fwd8_ws_bytes(s);
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int D, const fa_layout* layout, const fa_options* options,
+                     const float* descale_q, const float* descale_k, const float* descale_v,
+                     float scale, int causal, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  const Shape s{B, H, N, D};
+  return fwd8_impl(q, k, v, o, lse, s, layout ? from_abi(*layout) : contiguous_layout(s),
+                   options, descale_q, descale_k, descale_v, scale, causal, workspace,
+                   workspace_bytes, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic) {

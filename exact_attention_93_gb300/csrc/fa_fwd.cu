@@ -50,17 +50,21 @@ namespace fa {
 namespace {
 
 constexpr int kFwdThreads = 320;
-constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kFp8>
 struct FwdSmem {
-  static constexpr int kBlocks = D / 64;             // 64-element column blocks
-  static constexpr int kBlockBytes = kTile * 128;    // 128 rows x 128 B
+  static_assert(!kFp8 || D == 128, "8-bit operands: D = 128");
+  static constexpr int kRowBytes = kFp8 ? D : 2 * D;  // one Q or K row
+  static constexpr int kBlocks = kRowBytes / 128;      // 128-byte column blocks
+  static constexpr int kBlockBytes = kTile * 128;      // 128 rows x 128 B
   static constexpr int kTileBytes = kBlocks * kBlockBytes;
-  alignas(1024) uint8_t q[2][kTileBytes];  // tiles A and B; reused as O staging
+  static constexpr int kOBlocks = D / 64;              // 16-bit O: 64-column blocks
+  // tiles A and B; with 16-bit operands each is reused as its O staging
+  alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[2][kTileBytes];
-  alignas(1024) uint8_t v[2][kTileBytes];
+  alignas(1024) uint8_t v[2][kTileBytes];  // 8-bit: V^T, D rows x 128 keys
+  alignas(1024) uint8_t o[kFp8 ? 2 : 1][kFp8 ? kOBlocks * kBlockBytes : 16];
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
@@ -106,9 +110,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kSparse>
+// The two products in either operand width.
+template <bool kFp8>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                       uint32_t acc) {
+  if constexpr (kFp8)
+    tc_mma_ss_f8(d, a, b, id, acc);
+  else
+    tc_mma_ss(d, a, b, id, acc);
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                       uint32_t acc) {
+  if constexpr (kFp8)
+    tc_mma_ts_f8(d, a, b, id, acc);
+  else
+    tc_mma_ts(d, a, b, id, acc);
+}
+
+// kBf16: the 16-bit type of O (and of Q, K, V unless kFp8, where they are
+// e4m3 bytes and V arrives transposed).
+template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
-  using Smem = FwdSmem<D, kSparse>;
+  using Smem = FwdSmem<D, kSparse, kFp8>;
+  constexpr int kColsPerBlock = kFp8 ? 128 : 64;  // elements in a 128-byte block
+  // P = 2^(x - m + kPOffset) with the reference maximum m lagging the true
+  // one by at most kThreshold, so P < 2^(kThreshold + kPOffset) = 256.
+  // 16-bit P keeps the largest lag; 8-bit P (e4m3, largest finite 448,
+  // subnormal below 2^-6) spends half of it on the offset so that weights
+  // down to 2^-10 of the row maximum stay normal.
+  constexpr float kThreshold = kFp8 ? 4.0f : 8.0f;
+  constexpr float kPOffset = kFp8 ? 4.0f : 0.0f;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -191,8 +224,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       mbar_arrive_expect_tx(&s.q_full, n_q_here * Smem::kTileBytes);
       for (int t = 0; t < n_q_here; ++t)
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full, kb * 64,
-                      (2 * pt + t) * kTile, hh, bb);
+          tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full,
+                      kb * kColsPerBlock, (2 * pt + t) * kTile, hh, bb);
       int issued = 0;
       for (int j = walk.first(), jj = 0; j < walk.n; j = walk.next(j), ++jj) {
         const int st = jj & 1;  // jj: position in the stream
@@ -200,16 +233,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         if (jj >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
         for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st], kb * 64,
-                      j * kTile, hh, bb);
+          tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st],
+                      kb * kColsPerBlock, j * kTile, hh, bb);
         if (jj >= 2 && !mbar_wait(&s.v_empty[st], (u - 1) & 1, p.err, abort_flag)) {
           issued = jj * 2 + 1;
           break;
         }
         mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
-                      j * kTile, hh, bb);
+        if constexpr (kFp8) {
+          // V^T rows d = 0..D-1, keys j*128 .. j*128+127
+          tma_load_4d(s.v[st], &p.map_v, &s.v_full[st], j * kTile, 0, hh, bb);
+        } else {
+          for (int kb = 0; kb < Smem::kBlocks; ++kb)
+            tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
+                        j * kTile, hh, bb);
+        }
         issued = jj * 2 + 2;
       }
       if (*abort_flag) {
@@ -227,23 +265,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t ab = kBf16 ? 1u : 0u;
-      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
-      constexpr uint32_t idPV = idesc_f16(128, D, ab, 0, 1);
+      constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, ab, 0, 0);
+      // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
+      constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, D) : idesc_f16(128, D, ab, 0, 1);
       // Operand descriptors are built once and advanced by constant offsets.
       const uint64_t dq0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(smem_u32(s.v[0]), Smem::kBlockBytes, 1024);
+      const uint64_t dv0 =
+          smem_desc_sw128(smem_u32(s.v[0]), kFp8 ? 16 : Smem::kBlockBytes, 1024);
+      // One product step covers 32 bytes of each row: 16 elements of 16 bits,
+      // 32 of 8 bits.
+      constexpr int kStepElems = kFp8 ? 32 : 16;
       // S_t = Q_t K^T into tile t's S columns, K from stage kst
       auto issue_s = [&](int t, int kst) {
         const uint64_t dq = desc_add(dq0, t * Smem::kTileBytes);
         const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
           const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
-                    kk > 0 ? 1u : 0u);
+          mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
+                       kk > 0 ? 1u : 0u);
         }
         tc_commit(&s.s_full[t]);
+      };
+      // P step kk of V tile stage st: 16-bit V advances kStepElems rows of
+      // 128 bytes, 8-bit V^T 32 bytes within each row.
+      auto v_step = [](uint64_t dv, int kk) {
+        return kFp8 ? desc_add(dv, kk * 32) : desc_add(dv, kk * kStepElems * 128);
       };
       const int jf = walk.first();
       // with nothing to multiply (an empty block-sparse pair) no K arrives
@@ -278,9 +326,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               // O_t += P_t(j) V_j, with P read from tile t's S columns
               const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
-                          desc_add(dv, kk * 16 * 128), idPV, (j > lt || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                             idPV, (j > lt || kk > 0) ? 1u : 0u);
               tc_commit(&s.o_done[t]);
             }
             if (s_next) {
@@ -321,10 +369,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               tc_fence_after();
               // O_t += P_t(j) V_j, with P read from tile t's S columns
               const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-  #pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                tc_mma_ts(tbase + 256 + t * D, tbase + t * 128 + kk * 8,
-                          desc_add(dv, kk * 16 * 128), idPV, (ct > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                             idPV, (ct > 0 || kk > 0) ? 1u : 0u);
               tc_commit(&s.o_done[t]);
               if (t)
                 ++c1;
@@ -362,7 +410,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + t * 128, tO = tbase + 256 + t * D;
-    const float sl2 = p.scale_log2;
+    // 8-bit operands carry per-(batch, head) dequantisation factors: Q and K
+    // scale the scores, V scales O.
+    float sl2 = p.scale_log2, v_descale = 1.f;
+    if constexpr (kFp8) {
+      if (p.descale_q) sl2 *= p.descale_q[bh];
+      if (p.descale_k) sl2 *= p.descale_k[bh];
+      if (p.descale_v) v_descale = p.descale_v[bh];
+    }
     const bool pos_scale = sl2 > 0.f;
     float m = -INFINITY;  // reference maximum, log2 units
     float l = 0.f;        // running sum of 2^(t - m)
@@ -423,7 +478,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                              fmaxf(mxs[6], mxs[7]));
       const float m_tile = prescale ? mx : mx * sl2;
       const float m_new = fmaxf(m, m_tile);
-      const bool need = m_new > m + kRescaleThreshold;
+      const bool need = m_new > m + kThreshold;
       float alpha = 1.f;
       if (need) {
         alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
@@ -447,13 +502,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           tmem_st32(tO + lane_off + c * 32, o);
         }
       }
-      const float mneg = (m == -INFINITY) ? 0.f : -m;
+      const float mneg = (m == -INFINITY) ? 0.f : kPOffset - m;
       // P = 2^(x * mult - m), two columns per packed FMA / add; the softmax
       // warps share issue slots with the MMA warp, so fewer instructions
       // here keep the tensor core fed.
       const float mult = prescale ? 1.f : sl2;
       const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
       uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
+      uint32_t pk8[kFp8 ? 32 : 1];  // 8-bit P: four keys per column
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -463,10 +519,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               fma_f32x2(f32x2(sv[h * 64 + 2 * c], sv[h * 64 + 2 * c + 1]), mult2, mneg2));
           const float p0 = ex2_approx(z.x), p1 = ex2_approx(z.y);
           sums[c & 1] = add_f32x2(sums[c & 1], f32x2(p0, p1));
-          pk[c] = pack2<kBf16>(p0, p1);
+          if constexpr (kFp8) {
+            const uint32_t b2 = pack2_e4m3(p0, p1);
+            if (c & 1)
+              pk8[h * 16 + (c >> 1)] |= b2 << 16;
+            else
+              pk8[h * 16 + (c >> 1)] = b2;
+          } else {
+            pk[c] = pack2<kBf16>(p0, p1);
+          }
         }
-        tmem_st32(tS + lane_off + h * 32, pk);
+        if constexpr (!kFp8) tmem_st32(tS + lane_off + h * 32, pk);
       }
+      if constexpr (kFp8) tmem_st32(tS + lane_off, pk8);
       const float2 s0 = split_f32x2(sums[0]), s1 = split_f32x2(sums[1]);
       l += (s0.x + s0.y) + (s1.x + s1.y);
       tmem_st_wait();
@@ -486,8 +551,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                       : warp_wait(&s.q_full, 0, p.err, abort_flag));
       if (named_bar_and(1 + t, 128, mine)) {
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        uint8_t* stage = s.q[t];  // this tile's Q is no longer read
+        const float inv_l = l > 0.f ? v_descale / l : 0.f;
+        // 16-bit operands: this tile's Q is no longer read
+        uint8_t* stage = kFp8 ? s.o[t] : s.q[t];
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -515,14 +581,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
         if (r == 0) {
-          for (int kb = 0; kb < Smem::kBlocks; ++kb)
+          for (int kb = 0; kb < Smem::kOBlocks; ++kb)
             tma_store_4d(&p.map_o, stage + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
           tma_store_commit();
           tma_store_wait_all();
         }
         if (i < p.N)
           p.lse[static_cast<long long>(bh) * p.N + i] =
-              have ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+              have ? (m - kPOffset + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -535,10 +601,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   }
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kSparse>
+template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8 = false>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse>;
-  const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse>)) + 1024;
+  auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse, kFp8>;
+  const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse, kFp8>)) + 1024;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -552,7 +618,58 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// V^T for the 8-bit forward: the P V product wants its B operand K-major
+// (keys contiguous), so each (batch, head)'s [N, D] byte matrix is rewritten
+// as [D, ld] once per call.  A CTA moves one 128-key x 128-column tile; warp
+// w takes columns 16w .. 16w+15, lane l keys 4l .. 4l+3: four 16-byte row
+// loads, a 4 x 4 byte transpose per word (byte permutes) and sixteen 4-byte
+// stores, each warp-wide store covering 128 consecutive bytes of one V^T row.
+__global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __restrict__ v,
+                                                           RowStrides sv, uint8_t* __restrict__ vt,
+                                                           int N, long long ld, int H,
+                                                           int n_key_tiles) {
+  const int bh = static_cast<int>(blockIdx.x / n_key_tiles);
+  const int k0 = static_cast<int>(blockIdx.x % n_key_tiles) * kTile;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const long long b = bh / H, h = bh % H;
+  const uint8_t* src = v + b * sv.batch + h * sv.head + w * 16;
+  uint4 row[4];  // keys k0 + 4l + i, columns 16w .. 16w+15
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int key = k0 + 4 * l + i;
+    row[i] = key < N ? __ldg(reinterpret_cast<const uint4*>(src + key * sv.seq))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int kg = k0 + 4 * l;  // first key of this lane's group (a multiple of 4)
+  if (kg >= ld) return;       // ld is a multiple of 16: the group lies wholly inside
+  uint8_t* dst = vt + static_cast<long long>(bh) * 128 * ld + kg;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // columns 16w + 4c .. 16w + 4c + 3
+    const uint32_t w0 = (&row[0].x)[c], w1 = (&row[1].x)[c], w2 = (&row[2].x)[c],
+                   w3 = (&row[3].x)[c];
+    // rows of keys -> rows of columns
+    const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w0, w1, 0x7362);
+    const uint32_t t2 = __byte_perm(w2, w3, 0x5140), t3 = __byte_perm(w2, w3, 0x7362);
+    const uint32_t out[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632),
+                             __byte_perm(t1, t3, 0x5410), __byte_perm(t1, t3, 0x7632)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint32_t*>(dst + static_cast<long long>(16 * w + 4 * c + e) * ld) = out[e];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_v8(const void* v, RowStrides sv, void* vt, int N, long long ld, int H,
+                                long long BH, int D, cudaStream_t s) {
+  if (D != 128 || ld < N || (ld & 15) != 0) return cudaErrorInvalidValue;
+  const long long tiles = (N + kTile - 1) / kTile;
+  if (tiles * BH > INT_MAX) return cudaErrorInvalidConfiguration;
+  transpose_v8_kernel<<<static_cast<unsigned>(tiles * BH), 256, 0, s>>>(
+      static_cast<const uint8_t*>(v), sv, static_cast<uint8_t*>(vt), N, ld, H,
+      static_cast<int>(tiles));
+  return cudaGetLastError();
+}
 
 template <int D, bool kBf16>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
@@ -563,6 +680,15 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {
+  if (a.fp8) {
+    if (a.D != 128 || !a.bf16) return cudaErrorInvalidValue;
+    const bool alibi = a.band.alibi != nullptr, sparse = a.band.block_mask != nullptr;
+    if (sparse)
+      return alibi ? launch_fwd_t<128, true, true, true, true>(a, s)
+                   : launch_fwd_t<128, true, false, true, true>(a, s);
+    return alibi ? launch_fwd_t<128, true, true, false, true>(a, s)
+                 : launch_fwd_t<128, true, false, false, true>(a, s);
+  }
   if (a.D == 64) return a.bf16 ? launch_fwd_d<64, true>(a, s) : launch_fwd_d<64, false>(a, s);
   return a.bf16 ? launch_fwd_d<128, true>(a, s) : launch_fwd_d<128, false>(a, s);
 }

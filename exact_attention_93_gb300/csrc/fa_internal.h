@@ -32,13 +32,23 @@ struct Band {
 // sets live in shared memory as bitmasks).
 constexpr int kMaxSparseTiles = 16384;
 
+// 16-bit operands: every map has box 64 x 128 x 1 x 1, 128-byte swizzle.
+// 8-bit (e4m3) operands (fp8 != 0, D = 128, O in bf16): map_q and map_k
+// have box 128 x 128 bytes; map_v covers V^T, a [B][H][D][Npad16] byte
+// tensor with inner extent N, box 128 keys x D rows.
 struct FwdLaunch {
-  CUtensorMap map_q, map_k, map_v, map_o;  // box 64 x 128 x 1 x 1, 128B swizzle
+  CUtensorMap map_q, map_k, map_v, map_o;
   float* lse;                               // [BH][N]
   int N, BH, D, H;
   float scale_log2;                         // scale * log2(e)
   Band band;
   int bf16;
+  int fp8;
+  // 8-bit only: per-(batch, head) dequantisation factors, [BH] each, or
+  // nullptr for 1
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
   uint32_t* err;
 };
 
@@ -61,6 +71,11 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 struct RowStrides {
   long long batch, head, seq;
 };
+
+// V [B, H, N, D] bytes (element strides sv, D = 128) -> vt [BH][D][ld]
+// bytes, ld >= N a multiple of 16; columns N .. ld-1 are left as they are.
+cudaError_t launch_transpose_v8(const void* v, RowStrides sv, void* vt, int N, long long ld, int H,
+                                long long BH, int D, cudaStream_t s);
 
 cudaError_t launch_bwd_preprocess(const void* o, RowStrides so, const void* dO, RowStrides sdo,
                                   const float* lse, float* lse2, float* di, float* dq_accum, int N,

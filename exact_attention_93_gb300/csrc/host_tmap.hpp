@@ -48,19 +48,21 @@ inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS;
 }
 
-// A [batch][head][rows][inner] tensor of 16-bit elements with arbitrary
-// element strides for rows, heads and batches (inner contiguous).  Boxes are
-// box_inner x box_rows x 1 x 1; out-of-range rows read as zero and are not
-// written.  Returns false when the driver rejects the map (alignment, sizes).
+// A [batch][head][rows][inner] tensor of elem_bytes-byte elements with
+// arbitrary element strides for rows, heads and batches (inner contiguous).
+// Boxes are box_inner x box_rows x 1 x 1; out-of-range rows (and inner
+// elements) read as zero and are not written.  Returns false when the driver
+// rejects the map (alignment, sizes).
 inline bool make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
                          uint64_t inner, uint64_t rows, uint64_t heads, uint64_t batches,
                          uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride,
-                         uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+                         uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                         uint64_t elem_bytes = 2) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  constexpr uint64_t kElem = 2;
   cuuint64_t dims[4] = {inner, rows, heads, batches};
-  cuuint64_t strides[3] = {row_stride * kElem, head_stride * kElem, batch_stride * kElem};
+  cuuint64_t strides[3] = {row_stride * elem_bytes, head_stride * elem_bytes,
+                           batch_stride * elem_bytes};
   cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -81,6 +83,17 @@ inline bool operand_map(CUtensorMap* map, const void* base, bool bf16, int B, in
                       static_cast<uint64_t>(seq_stride), static_cast<uint64_t>(head_stride),
                       static_cast<uint64_t>(batch_stride), 64, static_cast<uint32_t>(box_rows),
                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// An 8-bit [B, H, N, D] operand (D = 128: one 128-byte row per box row).
+inline bool operand_map_u8(CUtensorMap* map, const void* base, int B, int H, int N, int D,
+                           long long batch_stride, long long head_stride, long long seq_stride,
+                           int box_rows) {
+  return make_tmap_4d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(D),
+                      static_cast<uint64_t>(N), static_cast<uint64_t>(H),
+                      static_cast<uint64_t>(B), static_cast<uint64_t>(seq_stride),
+                      static_cast<uint64_t>(head_stride), static_cast<uint64_t>(batch_stride),
+                      128, static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B, 1);
 }
 
 }  // namespace fa

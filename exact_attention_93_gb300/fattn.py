@@ -100,6 +100,9 @@ def load(path: str | None = None):
             "fa_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
                               ctypes.POINTER(FaLayout), ctypes.POINTER(FaOptions), f, i, i, i,
                               vp, sz, vp]),
+            "fa_fwd_fp8_workspace_size": (sz, [i, i, i, i]),
+            "fa_fwd_fp8": (i, [vp, vp, vp, vp, vp, i, i, i, i, ctypes.POINTER(FaLayout),
+                               ctypes.POINTER(FaOptions), vp, vp, vp, f, i, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -256,6 +259,60 @@ def fa_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, layout, opts, B: int, H: int, N: 
                           int(bool(deterministic)), _ptr(workspace), workspace.numel(),
                           _stream(stream))
     _check(st, "fa_bwd_ex")
+
+
+def _check_fp8(*ts):
+    torch = _torch()
+    for t in ts:
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"FP8 operands must be float8_e4m3fn (or their uint8 bytes), "
+                            f"got {t.dtype}")
+
+
+def _descale_ptr(t, B: int, H: int):
+    if t is None:
+        return None
+    torch = _torch()
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != B * H:
+        raise ValueError("descale factors must be contiguous float32 CUDA tensors of B*H "
+                         "elements ([B, H])")
+    return t.data_ptr()
+
+
+def fa_fwd_fp8_workspace_size(B: int, H: int, N: int, D: int) -> int:
+    return int(load().fa_fwd_fp8_workspace_size(B, H, N, D))
+
+
+def alloc_fp8_workspace(B, H, N, D, device=None):
+    """A 256-byte-aligned byte buffer of the size fa_fwd_fp8 needs."""
+    torch = _torch()
+    n = fa_fwd_fp8_workspace_size(B, H, N, D)
+    if n == 0:
+        raise ValueError("invalid sizes for an FP8 forward (D must be 128)")
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + n]
+
+
+def fa_fwd_fp8(q, k, v, o, lse, layout, opts, B: int, H: int, N: int, D: int, scale: float,
+               causal: bool, descale_q=None, descale_k=None, descale_v=None, workspace=None,
+               stream=None):
+    """fa_fwd_fp8: e4m3 q, k, v (float8_e4m3fn or uint8 bytes) in `layout`
+    (FaLayout or None for contiguous [B, H, N, D]); o bf16; optional [B, H]
+    float32 descale factors."""
+    _check_cuda(q, k, v, o, lse, workspace)
+    _check_fp8(q, k, v)
+    if o.dtype != _torch().bfloat16:
+        raise TypeError("the FP8 forward writes a bfloat16 O")
+    dq_, dk_, dv_ = (_descale_ptr(t, B, H) for t in (descale_q, descale_k, descale_v))
+    if workspace is None:
+        workspace = alloc_fp8_workspace(B, H, N, D, q.device)
+    st = load().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                           ctypes.byref(layout) if layout is not None else None,
+                           ctypes.byref(opts) if opts is not None else None,
+                           dq_, dk_, dv_, float(scale), int(bool(causal)), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
+    _check(st, "fa_fwd_fp8")
 
 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):

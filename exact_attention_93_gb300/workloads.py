@@ -100,6 +100,30 @@ def make_inputs(w: Workload, with_grad_output: bool | None = None):
     return out
 
 
+E4M3_MAX = 448.0  # largest finite e4m3 value
+
+
+def make_fp8_inputs(w: Workload):
+    """Seeded e4m3 inputs for the FP8 forward: Q, K, V drawn exactly as
+    ``make_inputs`` draws them (float32 standard normals, same generator and
+    order), then scaled per (b, h) so that the largest magnitude maps to 448
+    and rounded to torch.float8_e4m3fn (round to nearest even).  Returns CPU
+    tensors q8, k8, v8 [B, H, N, D] and the float32 [B, H] factors
+    descale_q, descale_k, descale_v (amax / 448) that map the bytes back to
+    the drawn scale."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.D)
+    out = {}
+    for name in ("q", "k", "v"):
+        x = torch.randn(shape, dtype=torch.float32, generator=g)
+        amax = x.abs().amax(dim=(2, 3)).clamp_min(1e-30)
+        descale = (amax / E4M3_MAX).to(torch.float32)
+        out[name + "8"] = (x / descale[:, :, None, None]).to(torch.float8_e4m3fn)
+        out["descale_" + name] = descale.contiguous()
+    return out
+
+
 def custom(B, H, N, D, dtype="bf16", causal=False, seed=0, backward=True,
            do_std=1.0) -> Workload:
     """A workload of any shape (edge cases in the tests)."""

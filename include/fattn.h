@@ -15,6 +15,9 @@
  *          backward recomputation, v2 sequence-dimension parallelism.
  *   [API]  claire-chang.com FlashAttention introduction: the flash_attn_func
  *          argument list (softmax_scale, causal, deterministic).
+ *   [WIKI] "Flash Attention" wiki page (aiboss88.com): implementation
+ *          section, FlashAttention-3's FP8 forward; [DEEP] v1 -> v3 table
+ *          (v3 adds FP8).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -55,7 +58,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, bad scale   */
-  FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, unknown dtype                 */
+  FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128} (FP8: not 128), unknown dtype  */
   FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed              */
   FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait                */
 } fa_status;
@@ -157,6 +160,48 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int H, int N, int D, const fa_layout* layout, const fa_options* options,
                     float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Workspace bytes fa_fwd_fp8 needs: B*H*D*ld bytes (V transposed, ld = N
+ * rounded up to 16), rounded up to 256.  Returns 0 for invalid sizes or
+ * D != 128.
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int D);
+
+/*
+ * FP8 forward ([WIKI] implementation section; [DEEP] v3): fa_fwd_ex with Q,
+ * K and V given as e4m3 bytes (OCP FP8 E4M3: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, largest finite 448, no infinities) and
+ * per-(batch, head) dequantisation factors:
+ *
+ *   Q~ = descale_q[b,h] * Q,  K~ = descale_k[b,h] * K,  V~ = descale_v[b,h] * V
+ *   o, lse = the fa_fwd_ex result for Q~, K~, V~   (o in bf16)
+ *
+ *   q, k, v     device, e4m3 bytes [B, H, N, D] in `layout` (strides in
+ *               bytes, multiples of 16; NULL: contiguous).  D must be 128
+ *               (FA_ERR_UNSUPPORTED otherwise).
+ *   o           device, bf16 [B, H, N, D] in layout->o (elements, multiples
+ *               of 8).   lse: device fp32 [B, H, N], natural log.
+ *   descale_*   NULL (factor 1) or device fp32 [B][H], 4-byte aligned, read
+ *               by the kernels and not validated (finite values expected).
+ *   options     window, ALiBi and block mask exactly as for fa_fwd_ex.
+ *   workspace   device, fa_fwd_fp8_workspace_size(...) bytes, 256-byte
+ *               aligned; overwritten (it holds V transposed to [B,H,D,ld]).
+ *
+ * Scores and the softmax statistics are exact products accumulated in
+ * fp32, as for 16-bit inputs.  The probabilities P enter the P V product
+ * rounded to e4m3, each relative to the row maximum known when its tile is
+ * processed and scaled by a power of two so that weights down to 2^-10 of
+ * that maximum stay normal; the row sum uses the unrounded P.  So o differs
+ * from the exact result by at most about 2^-4 of sum_j P_ij |V~_jd| (the
+ * e4m3 half-ulp) plus the bf16 rounding of o; lse carries no P rounding.
+ * Deterministic: the same inputs give bit-identical outputs.
+ */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int D, const fa_layout* layout, const fa_options* options,
+                     const float* descale_q, const float* descale_k, const float* descale_v,
+                     float scale, int causal, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /*
  * Workspace bytes fa_bwd needs, laid out as (each part 256-byte aligned):

@@ -69,6 +69,8 @@ def _bind(path: str):
         ctypes.POINTER(ctypes.c_ubyte), ctypes.c_long, lp, ctypes.c_long,
         dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, dp, dp,
     ]
+    lib.fa_oracle_rows_p.restype = ctypes.c_int
+    lib.fa_oracle_rows_p.argtypes = list(lib.fa_oracle_rows_bs.argtypes) + [dp]
     lib.fa_oracle_threads.restype = ctypes.c_int
     lib.fa_oracle_threads.argtypes = []
     lib.fa_oracle_set_threads.restype = None
@@ -114,7 +116,7 @@ def _ptr(a):
 
 def attention_head(q, k, v, scale, causal, dout=None, rows=None,
                    kv_range=None, want_grads=True, window=(-1, -1), alibi_slope=0.0,
-                   block_mask=None, block=128):
+                   block_mask=None, block=128, want_probs=False):
     """Exact attention for one (batch, head) slice.
 
     q, k, v, dout: [N, D].  rows: query-row indices (default: all rows).
@@ -126,8 +128,9 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
     [ceil(N / block), ceil(N / block)] array; key j is visible to query i
     only where block_mask[i // block, j // block] is nonzero.
 
-    Returns a dict with o [R, D], lse [R] and, when dout is given, dq [R, D],
-    di [R] and (if a key range applies) dk, dv [end - begin, D].
+    Returns a dict with o [R, D], lse [R], p [R, N] (the probability rows,
+    when want_probs) and, when dout is given, dq [R, D], di [R] and (if a key
+    range applies) dk, dv [end - begin, D].
     """
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -163,16 +166,19 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
         bm = np.ascontiguousarray(np.asarray(block_mask) != 0, dtype=np.uint8)
         if bm.shape != (nb, nb):
             raise ValueError(f"block_mask must be [{nb}, {nb}] for N = {N}, block = {block}")
-    rc = lib.fa_oracle_rows_bs(
+    probs = np.empty((R, N), np.float64) if want_probs else None
+    rc = lib.fa_oracle_rows_p(
         _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, D, float(scale), int(bool(causal)),
         left, right, float(alibi_slope),
         bm.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)) if bm is not None else None,
         int(block),
         rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if rows_arr is not None else None,
-        R, _ptr(o), _ptr(lse), _ptr(dq), _ptr(di), kb, ke, _ptr(dk), _ptr(dv))
+        R, _ptr(o), _ptr(lse), _ptr(dq), _ptr(di), kb, ke, _ptr(dk), _ptr(dv), _ptr(probs))
     if rc != 0:
-        raise RuntimeError(f"fa_oracle_rows_bs failed with code {rc}")
+        raise RuntimeError(f"fa_oracle_rows_p failed with code {rc}")
     out = {"o": o, "lse": lse}
+    if probs is not None:
+        out["p"] = probs
     if dq is not None:
         out["dq"] = dq
         out["di"] = di
@@ -183,7 +189,8 @@ def attention_head(q, k, v, scale, causal, dout=None, rows=None,
 
 
 def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None,
-              window=(-1, -1), alibi_slopes=None, block_mask=None, block=128):
+              window=(-1, -1), alibi_slopes=None, block_mask=None, block=128,
+              want_probs=False):
     """Exact attention over a [B, H, N, D] batch, one (b, h) slice at a time.
 
     rows: None (every row) or a callable (b, h) -> row indices, or an array of
@@ -209,7 +216,7 @@ def attention(q, k, v, scale, causal, dout=None, rows=None, kv_range=None,
                                  kv_range, window=window, alibi_slope=slopes[b, h],
                                  block_mask=None if block_mask is None else
                                  (block_mask[h] if np.ndim(block_mask) == 3 else block_mask),
-                                 block=block)
+                                 block=block, want_probs=want_probs)
             for key, val in one.items():
                 res.setdefault(key, []).append(val)
     for key in list(res):

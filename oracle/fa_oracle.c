@@ -185,6 +185,18 @@ int fa_oracle_rows_bs(const double* q, const double* k, const double* v,
                       const long* rows, long nrows, double* o, double* lse,
                       double* dq, double* di, long kv_begin, long kv_end,
                       double* dk, double* dv) {
+    return fa_oracle_rows_p(q, k, v, dout, N, D, scale, causal, left, right,
+                            slope, mask, tile, rows, nrows, o, lse, dq, di,
+                            kv_begin, kv_end, dk, dv, NULL);
+}
+
+int fa_oracle_rows_p(const double* q, const double* k, const double* v,
+                     const double* dout, long N, long D, double scale,
+                     int causal, long left, long right, double slope,
+                     const unsigned char* mask, long tile,
+                     const long* rows, long nrows, double* o, double* lse,
+                     double* dq, double* di, long kv_begin, long kv_end,
+                     double* dk, double* dv, double* p) {
     if (!q || !k || !v || !o || !lse || N < 1 || D < 1 || nrows < 0)
         return 1;
     if (left < -1 || right < -1 || !isfinite(slope)) return 1;
@@ -259,6 +271,7 @@ int fa_oracle_rows_bs(const double* q, const double* k, const double* v,
         }
     }
 
+    if (p) memcpy(p, p_all, sizeof(double) * (size_t)nrows * (size_t)N);
     free(p_all);
     free(ds_all);
     free(s_all);

@@ -57,6 +57,18 @@ int fa_oracle_rows_bs(const double* q, const double* k, const double* v,
                       double* dq, double* di, long kv_begin, long kv_end,
                       double* dk, double* dv);
 
+/*
+ * fa_oracle_rows_bs that also returns the probability rows: p (may be NULL)
+ * is [nrows, N], p[r][j] = P_ij for query i = rows[r] (0 where masked).
+ */
+int fa_oracle_rows_p(const double* q, const double* k, const double* v,
+                     const double* dout, long N, long D, double scale,
+                     int causal, long left, long right, double slope,
+                     const unsigned char* mask, long tile,
+                     const long* rows, long nrows, double* o, double* lse,
+                     double* dq, double* di, long kv_begin, long kv_end,
+                     double* dk, double* dv, double* p);
+
 /* OpenMP threads the next call will use, and a way to set them. */
 int fa_oracle_threads(void);
 void fa_oracle_set_threads(int n);

@@ -12,7 +12,8 @@ NULL = None
 EXPECTED = [
     "fa_abi_version", "fa_bwd", "fa_bwd_dkdv", "fa_bwd_dq", "fa_bwd_dq_convert", "fa_bwd_noalloc",
     "fa_bwd_ex", "fa_bwd_preprocess", "fa_bwd_strided", "fa_bwd_workspace_size", "fa_device_error",
-    "fa_fwd", "fa_fwd_ex", "fa_fwd_strided", "fa_selftest_wait_timeout", "fa_status_string",
+    "fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_fp8_workspace_size", "fa_fwd_strided",
+    "fa_selftest_wait_timeout", "fa_status_string",
 ]
 
 
@@ -36,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 4
+    assert lib.fa_abi_version() == 5
     names = [lib.fa_status_string(i).decode() for i in range(5)]
     assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
                      "FA_ERR_TIMEOUT"]
@@ -202,3 +203,52 @@ def test_block_mask_beyond_the_tile_limit_is_unsupported(lib):
     N = 128 * 16384 + 1                      # 16385 tiles along N
     assert lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, N, 64, None, ctypes.byref(opt),
                          ctypes.c_float(0.125), 0, 0, NULL) == fattn.FA_ERR_UNSUPPORTED
+
+
+def fwd8(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=300, D=128, layout=None,
+         opts=None, dq=None, dk=None, dv=None, scale=0.09, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.fa_fwd_fp8_workspace_size(B, H, N, 128)
+    return lib.fa_fwd_fp8(q, k, v, o, lse, B, H, N, D,
+                          ctypes.byref(layout) if layout is not None else None,
+                          ctypes.byref(opts) if opts is not None else None, dq, dk, dv,
+                          ctypes.c_float(scale), 0, ws, ws_bytes, NULL)
+
+
+def test_fp8_workspace_size(lib):
+    # V^T: B*H*D*ld bytes, ld = N rounded up to 16, rounded up to 256
+    assert lib.fa_fwd_fp8_workspace_size(1, 2, 300, 128) == 2 * 128 * 304
+    assert lib.fa_fwd_fp8_workspace_size(3, 1, 1, 128) == 3 * 128 * 16
+    assert lib.fa_fwd_fp8_workspace_size(1, 1, 128, 64) == 0     # D must be 128
+    assert lib.fa_fwd_fp8_workspace_size(0, 1, 128, 128) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"D": 64}, fattn.FA_ERR_UNSUPPORTED),
+    ({"q": NULL}, fattn.FA_ERR_INVALID_ARG),
+    ({"k": FAKE + 8}, fattn.FA_ERR_INVALID_ARG),
+    ({"N": 0}, fattn.FA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, fattn.FA_ERR_INVALID_ARG),
+    ({"dv": FAKE + 2}, fattn.FA_ERR_INVALID_ARG),          # descale not 4-byte aligned
+    ({"ws": NULL}, fattn.FA_ERR_INVALID_ARG),
+    ({"ws": FAKE + 16}, fattn.FA_ERR_INVALID_ARG),          # workspace not 256-byte aligned
+    ({"ws_bytes": 2 * 128 * 304 - 1}, fattn.FA_ERR_INVALID_ARG),
+    # 8-bit operand strides are bytes and must be multiples of 16
+    ({"layout": fattn.FaLayout(fattn.FaStrides(2 * 300 * 128, 300 * 128, 136),
+                               *([fattn.FaStrides(2 * 300 * 128, 300 * 128, 128)] * 7))},
+     fattn.FA_ERR_INVALID_ARG),
+    ({"layout": fattn.FaLayout(*([fattn.FaStrides(2 * 300 * 128, 300 * 128, 128)] * 2),
+                               fattn.FaStrides(2 * 300 * 128, 8, 128),
+                               *([fattn.FaStrides(2 * 300 * 128, 300 * 128, 128)] * 5))},
+     fattn.FA_ERR_INVALID_ARG),
+    ({"opts": fattn.FaOptions(-3, 0, None, 0, None, 0)}, fattn.FA_ERR_INVALID_ARG),
+])
+def test_fp8_forward_rejects_bad_arguments(lib, kw, status):
+    assert fwd8(lib, **kw) == status
+
+
+def test_fp8_binding_checks_types():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fattn.fa_fwd_fp8(x, x, x, x, x, None, None, 1, 1, 128, 128, 0.1, False)  # CPU tensors
