@@ -26,6 +26,7 @@ import io
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -51,6 +52,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the forward-only long-context measurement")
+    ap.add_argument("--fp8-only", action="store_true",
+                    help="time only the FP8 forward (fa_fwd_fp8) on e4m3 draws of the workload")
     return ap.parse_args()
 
 
@@ -83,10 +86,23 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def kernel_source_hash():
+def code_text(src: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed: the
+    part of a file that decides what the compiler builds."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_source_hash(sources: dict | None = None):
+    """sha256 prefix over the code of every file in csrc/ (comments and
+    whitespace ignored), or of `sources` ({file name: text})."""
+    if sources is None:
+        d = os.path.join(ROOT, "exact_attention_93_gb300", "csrc")
+        sources = {f: open(os.path.join(d, f), encoding="utf-8").read() for f in os.listdir(d)}
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "exact_attention_93_gb300", "csrc"))):
-        h.update(open(os.path.join(ROOT, "exact_attention_93_gb300", "csrc", f), "rb").read())
+    for name in sorted(sources):
+        h.update(name.encode() + b"\0" + code_text(sources[name]).encode() + b"\0")
     return h.hexdigest()[:16]
 
 
@@ -317,7 +333,7 @@ def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
     return out
 
 
-def fp8_extras(w, dev, stream, pk):
+def fp8_extras(w, dev, stream, pk, reps=10, warmup=3):
     """The FP8 forward (fa_fwd_fp8: the V transpose plus the forward kernel)
     on e4m3 draws of the benchmark shape, against the e4m3 peak taken as
     twice the measured bf16 one (the nominal dense ratio, 4.5 / 2.25 PFLOP/s)."""
@@ -335,11 +351,10 @@ def fp8_extras(w, dev, stream, pk):
         fattn.fa_fwd_fp8(d["q8"], d["k8"], d["v8"], o, lse, None, None, B, H, N, D, w.scale,
                          w.causal, d["descale_q"], d["descale_k"], d["descale_v"], ws)
 
-    for _ in range(3):
+    for _ in range(warmup):
         one()
     torch.cuda.synchronize()
     s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 10
     s0.record(stream)
     for _ in range(reps):
         one()
@@ -354,6 +369,22 @@ def fp8_extras(w, dev, stream, pk):
         "peak": 2.0 * pk["sustained"],
         "peak_source": f"{pk['source']} bf16 sustained x 2 (nominal e4m3 / bf16 ratio)",
         "note": "fa_fwd_fp8 (V transpose + forward), O in bf16, per-head descale factors"}}
+
+
+def run_fp8_only(args, w):
+    """One JSON line for the FP8 forward alone (profiling and sweeps)."""
+    import torch
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    res = fp8_extras(w, dev, torch.cuda.current_stream(), peaks(), reps=args.steps,
+                     warmup=max(args.warmup, 3))
+    (label, r), = res.items()
+    print(json.dumps({"metric": "e4m3 attention forward TFLOP/s", "value": r["tflops"],
+                      "unit": "TFLOP/s", "ms": r["ms"], "workload": label,
+                      "frac_of_e4m3_peak": r["frac_of_e4m3_peak"], "steps": args.steps}),
+          flush=True)
 
 
 def run_ours(args, w):
@@ -563,6 +594,8 @@ def main():
         raise SystemExit(f"workload {args.workload} has no backward; pick one that does")
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.fp8_only:
+        run_fp8_only(args, w)
     else:
         run_ours(args, w)
 

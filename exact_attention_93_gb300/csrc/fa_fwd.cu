@@ -40,6 +40,14 @@
 // (flash_attn_func alibi_slopes) every score gets -slope * |i - j| added
 // before the softmax.  The grid runs head-major, the longest query-tile
 // pairs of a head first, so the CTAs in flight share one head's K and V in L2.
+//
+// 8-bit operands (the FP8 forward FlashAttention-3 adds, which the "Flash
+// Attention" wiki page and the v3 row of "FlashAttention 深入" list): Q, K
+// and V^T arrive as e4m3 bytes, both products run as kind::f8f6f4 (K = 32
+// per step), P goes into TMEM as e4m3 (four keys per column) at a scale
+// that keeps it below 256 and small weights normal, and O leaves in bf16
+// through its own staging buffers.  Per-(batch, head) descale factors scale
+// the scores (Q, K) and O (V).
 #include <climits>
 
 #include "fa_band.cuh"
