@@ -54,6 +54,8 @@ def parse():
                     help="skip the forward-only long-context measurement")
     ap.add_argument("--fp8-only", action="store_true",
                     help="time only the FP8 forward (fa_fwd_fp8) on e4m3 draws of the workload")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time only the forward (fa_fwd) on the workload")
     return ap.parse_args()
 
 
@@ -371,6 +373,100 @@ def fp8_extras(w, dev, stream, pk, reps=10, warmup=3):
         "note": "fa_fwd_fp8 (V transpose + forward), O in bf16, per-head descale factors"}}
 
 
+# exp2 throughput of GB300's special-function unit: ex2.approx.ftz.f32
+# measured at 32 lanes per clock per SM (all-SM probe)
+EX2_PER_CLK_SM = 32
+
+
+def exp_count(w) -> float:
+    """Exponentials one forward evaluates: one per visible (query, key) pair,
+    B*H*N^2, halved under the causal mask; the backward evaluates as many
+    again when it recomputes P."""
+    n = float(w.B) * w.H * w.N * w.N
+    return n / 2 if w.causal else n
+
+
+def exp_peak(sm_mhz: float) -> float:
+    return EX2_PER_CLK_SM * 152 * sm_mhz * 1e6
+
+
+def time_calls(fn, reps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(reps):
+        fn()
+    e0.record(stream)
+    torch.cuda.synchronize()
+    return s0.elapsed_time(e0) / reps
+
+
+def small_config_extras(dev, stream, pk):
+    """Forward and forward + backward (atomic dQ) of the two D = 64
+    workloads, B8 H12 N1024 causal bf16 and B32 H16 N512 fp16, whose inputs
+    fit in L2 (back-to-back calls)."""
+    import torch
+
+    from exact_attention_93_gb300 import fattn, workloads as W
+
+    out = {}
+    for name in ("gpt2_causal", "bert_fp16"):
+        w = W.WORKLOADS[name]
+        g = {k: v.to(dev) for k, v in W.make_inputs(w).items()}
+        o = torch.empty_like(g["q"])
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+        ws = fattn.alloc_workspace(w.B, w.H, w.N, w.D, False, dev)
+
+        def fwd():
+            fattn.fa_fwd(g["q"], g["k"], g["v"], o, lse, w.scale, w.causal)
+
+        def step():
+            fwd()
+            fattn.fa_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], dq, dk, dv, w.scale, w.causal,
+                         False, ws)
+
+        ms_f = time_calls(fwd, 50, 5, stream)
+        ms_s = time_calls(step, 50, 5, stream)
+        tf_f = w.fwd_flops() / (ms_f * 1e-3) / 1e12
+        tf_s = (w.fwd_flops() + w.bwd_flops()) / (ms_s * 1e-3) / 1e12
+        out[f"{w.describe()} fwd"] = {"tflops": tf_f, "ms": ms_f, "frac_of_peak": tf_f / pk["burst"],
+                                      "peak_source": f"{pk['source']} bf16 burst"}
+        out[f"{w.describe()} fwd+bwd"] = {
+            "tflops": tf_s, "ms": ms_s, "frac_of_peak": tf_s / pk["burst"],
+            "peak_source": f"{pk['source']} bf16 burst",
+            "note": "fa_fwd + fa_bwd (atomic dQ), back-to-back calls; inputs fit in L2"}
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the D = 64 runs")
+    return out
+
+
+def run_fwd_only(args, w):
+    """One JSON line for the 16-bit forward alone (profiling and sweeps)."""
+    import torch
+
+    from exact_attention_93_gb300 import fattn, workloads as W
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g = {k: v.to(dev) for k, v in W.make_inputs(w, with_grad_output=False).items()}
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: fattn.fa_fwd(g["q"], g["k"], g["v"], o, lse, w.scale, w.causal),
+                    args.steps, max(args.warmup, 3), torch.cuda.current_stream())
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+    pk = peaks()
+    print(json.dumps({"metric": "attention forward TFLOP/s", "value": tf, "unit": "TFLOP/s",
+                      "ms": ms, "workload": w.describe(), "frac_of_burst_peak": tf / pk["burst"],
+                      "exp_per_s": exp_count(w) / (ms * 1e-3), "steps": args.steps}), flush=True)
+
+
 def run_fp8_only(args, w):
     """One JSON line for the FP8 forward alone (profiling and sweeps)."""
     import torch
@@ -544,6 +640,7 @@ def run_ours(args, w):
                                          "note": "back-to-back launches; inputs 16.8 MB each fit in L2"}
         extra.update(band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk))
         extra.update(fp8_extras(w, dev, stream, pk))
+        extra.update(small_config_extras(dev, stream, pk))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -551,6 +648,16 @@ def run_ours(args, w):
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{nrows} query rows of {w.describe()} ({nrows // w.H} per head), "
                          f"each row's whole forward and backward share, fp64, {dt:.1f} s"}
+
+    # the secondary ceiling: exponentials per second against the unit's rate
+    clk_summary = clk.summary()
+    mhz = clk_summary.get("sm_mhz") or 2070.0
+    n_exp = exp_count(w)
+    exp_rate = {"fwd": n_exp / (per_kernel["fwd"] * 1e-3),
+                "bwd_dkdv": n_exp / (per_kernel["bwd_dkdv"] * 1e-3),
+                "unit": "exp/s", "peak": exp_peak(mhz),
+                "peak_source": f"{EX2_PER_CLK_SM} ex2 lanes/clk/SM (measured) x 152 SMs x {mhz:.0f} MHz"}
+    exp_rate["frac_fwd"] = exp_rate["fwd"] / exp_rate["peak"]
 
     launches = len(names) * args.steps  # one kernel per entry-point call
     if rank == 0:
@@ -569,11 +676,12 @@ def run_ours(args, w):
             "frac_of_peak": {"fwd+bwd": value / world / peak_sust, "fwd": fwd_tf / peak_sust,
                              "peak": peak_sust, "peak_source": f"{pk['source']} bf16 sustained"},
             "kernel_ms": per_kernel,
+            "exp_rate": exp_rate,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
-            "clocks": clk.summary(),
+            "clocks": clk_summary,
             "extra": extra,
         }
         print(json.dumps(line), flush=True)
@@ -590,12 +698,16 @@ def main():
                      seed=4)
     else:
         w = W.WORKLOADS[args.workload]
-    if not w.backward:
-        raise SystemExit(f"workload {args.workload} has no backward; pick one that does")
     if args.impl == "reference":
+        if not w.backward:
+            raise SystemExit(f"workload {args.workload} has no backward; pick one that does")
         run_reference(args, w)
     elif args.fp8_only:
         run_fp8_only(args, w)
+    elif args.fwd_only:
+        run_fwd_only(args, w)
+    elif not w.backward:
+        raise SystemExit(f"workload {args.workload} has no backward; use --fwd-only")
     else:
         run_ours(args, w)
 

@@ -7,20 +7,19 @@
 //               softmax Jacobian; LSE rescaled to log2 units; both padded to
 //               whole 128-row tiles (+inf / 0) so the tile kernels can copy
 //               them with one bulk copy.  Also zeroes the fp32 dQ accumulator.
-//   dkdv        one CTA per 128-key tile, looping over 128-query tiles:
+//   dkdv        one CTA per 128-key tile, software-pipelined over 64-row
+//               query tiles (D = 64 or 128):
 //                 S^T  = K Q^T            (TMEM)      P^T = exp2(S^T*c - lse2)
 //                 dP^T = V dO^T           (TMEM)      dS^T = P^T (dP^T - Di)
-//                 dV  += P^T dO           (A = P^T written back into TMEM)
-//                 dK  += dS^T Q           (A = dS^T in swizzled smem)
-//                 dQ_i = dS K             (atomic mode; A = dS^T read MN-major)
-//               dQ rows are added to an fp32 accumulator with vector atomics.
+//                 dV  += P^T dO           (A = P^T packed into TMEM)
+//                 dK  += dS^T Q           (A = dS^T packed into TMEM)
+//                 dQ^T = K^T dS^T         (atomic mode, into TMEM; drained
+//                                          with fp32 atomics)
 //   dq          deterministic mode: one CTA per 128-query tile looping over
 //               key tiles, dQ accumulated in TMEM, no atomics.
 //   dq_convert  dQ = scale * accumulator, rounded to the input type.
 //
-// Warp roles in the tile kernels (192 threads): warps 0-3 elementwise work,
-// one TMEM lane (one tile row) per thread; warp 4 TMA producer; warp 5 MMA
-// issuer.  Every wait is bounded.
+// Every wait is bounded.
 #include <climits>
 
 #include "fa_band.cuh"
@@ -30,7 +29,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;  // deterministic dQ kernel
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
@@ -46,12 +45,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
           "r"(smem_u32(smem_dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
 }
 
 // Write 32 consecutive 16-bit values (16 packed words) of tile row r,
@@ -120,304 +113,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 }
 
 // ---------------------------------------------------------------------------
-// dK / dV (and atomic dQ)
-// ---------------------------------------------------------------------------
-template <int D, bool kSparse>
-struct DkdvSmem {
-  static constexpr int kBlocks = D / 64;
-  static constexpr int kBlockBytes = kTile * 128;
-  static constexpr int kTileBytes = kBlocks * kBlockBytes;
-  alignas(1024) uint8_t k[kTileBytes];
-  alignas(1024) uint8_t v[kTileBytes];
-  alignas(1024) uint8_t q[kTileBytes];   // reused for the dK output tile
-  alignas(1024) uint8_t dO[kTileBytes];  // reused for the dV output tile
-  alignas(1024) uint8_t dst[2 * kBlockBytes];  // dS^T: 128 keys x 128 queries
-  alignas(16) float lse2[kTile];
-  alignas(16) float di[kTile];
-  uint64_t kv_full, qdo_full, qdo_empty, s_full, p_full, mma_done, tmem_free, drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  uint32_t q_tiles[kSparse ? kMaxSparseTiles / 32 : 1];  // block-sparse: query tiles
-};
-
-template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdLaunch p) {
-  using Smem = DkdvSmem<D, kSparse>;
-  extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                     ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (p.N + kTile - 1) / kTile;
-  const int Npad = n_tiles * kTile;
-  // Head-major; key tiles near the start see the most queries and go first.
-  const int bh = static_cast<int>(blockIdx.x / n_tiles);
-  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
-  const int kt = static_cast<int>(blockIdx.x % n_tiles);
-  const int k0 = kt * kTile;
-  const int wl = p.band.win_left, wr = p.band.win_right;
-  int it_begin, it_last;  // query tiles whose band reaches this key tile
-  band_query_tiles(k0, kTile, kTile, n_tiles, wl, wr, it_begin, it_last);
-  const TileWalk<kSparse> walk{it_begin, it_last, n_tiles, TileSet{s.q_tiles, n_tiles}};
-  if constexpr (kSparse)
-    fill_tile_set(s.q_tiles, n_tiles, [&](int it) {
-      return it >= it_begin && it <= it_last && block_kept(p.band, bh, p.H, n_tiles, it, kt);
-    });
-  __syncthreads();
-  const int n_it = walk.count();
-
-  if (tid == 0) {
-    mbar_init(&s.kv_full, 1);
-    mbar_init(&s.qdo_full, 1);
-    mbar_init(&s.qdo_empty, 1);
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.mma_done, 1);
-    mbar_init(&s.tmem_free, 128);
-    mbar_init(&s.drain, 1);
-    s.abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 4) {
-    tmem_alloc(&s.tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = s.tmem_base;
-  const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + D;
-  const uint32_t tdQ = tbase;  // aliases S^T once it has been consumed
-  volatile int* abort_flag = &s.abort_flag;
-
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&s.kv_full, 2 * Smem::kTileBytes);
-      for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-        tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.kv_full, kb * 64, k0, hh, bb);
-        tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
-      }
-      int issued = 0;
-      for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-        const int q0 = qt * kTile;
-        if (it >= 1 && !mbar_wait(&s.qdo_empty, (it - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes + 2 * kTile * 4);
-        for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-          tma_load_4d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, hh, bb);
-          tma_load_4d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, hh, bb);
-        }
-        const long long off = static_cast<long long>(bh) * Npad + q0;
-        bulk_load(s.lse2, p.lse + off, kTile * 4, &s.qdo_full);
-        bulk_load(s.di, p.di + off, kTile * 4, &s.qdo_full);
-        issued = it + 1;
-      }
-      if (*abort_flag) {
-        int zero = 0;
-        mbar_wait(&s.kv_full, 0, p.err, &zero, 100000000ull);
-        if (issued > 0) mbar_wait(&s.qdo_full, (issued - 1) & 1, p.err, &zero, 100000000ull);
-      }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t ab = kBf16 ? 1u : 0u;
-      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);   // K-major A and B
-      constexpr uint32_t idKM = idesc_f16(128, D, ab, 0, 1);    // A K-major, B MN-major
-      constexpr uint32_t idMM = idesc_f16(128, D, ab, 1, 1);    // both MN-major
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
-      const uint32_t dst_addr = smem_u32(s.dst);
-      bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
-      for (int it = 0; ok && it < n_it; ++it) {
-        if (!mbar_wait(&s.qdo_full, it & 1, p.err, abort_flag)) break;
-        if (kAtomicDq && it >= 1 && !mbar_wait(&s.tmem_free, (it - 1) & 1, p.err, abort_flag))
-          break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tS, desc_add(smem_desc_sw128(k_addr, 16, 1024), off),
-                    desc_add(smem_desc_sw128(q_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdP, desc_add(smem_desc_sw128(v_addr, 16, 1024), off),
-                    desc_add(smem_desc_sw128(do_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s.s_full);
-        if (!mbar_wait(&s.p_full, it & 1, p.err, abort_flag)) break;
-        tc_fence_after();
-        // dV += P^T dO : A = P^T in TMEM (16-bit pairs over S^T columns [0, 64))
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tdV, tS + kk * 8, desc_add(smem_desc_sw128(do_addr, Smem::kBlockBytes, 1024), kk * 16 * 128),
-                    idKM, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q : A = dS^T in smem, K-major over queries
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdK, desc_add(smem_desc_sw128(dst_addr, 16, 1024), aoff),
-                    desc_add(smem_desc_sw128(q_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idKM,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (kAtomicDq) {
-          // dQ_i = dS K : A = dS (queries x keys) read MN-major from dS^T
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_ss(tdQ, desc_add(smem_desc_sw128(dst_addr, Smem::kBlockBytes, 1024), kk * 16 * 128),
-                      desc_add(smem_desc_sw128(k_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idMM,
-                      kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s.mma_done);
-        tc_commit(&s.qdo_empty);
-      }
-      tc_commit(&s.drain);
-      int zero = 0;
-      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
-    }
-  } else {
-    // ------------------------------------------------------------ elementwise
-    const int r = tid;  // key row within the tile (TMEM lane)
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const float sl2 = p.scale_log2;
-    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
-    bool ok = true;
-    for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-      const int q0 = qt * kTile;
-      if (!warp_wait(&s.s_full, it & 1, p.err, abort_flag) ||
-          !warp_wait(&s.qdo_full, it & 1, p.err, abort_flag)) {  // lse2 / Di of this tile
-        ok = false;
-        break;
-      }
-      // dS^T smem of the previous tile must have been consumed
-      if (!kAtomicDq && it >= 1 && !warp_wait(&s.mma_done, (it - 1) & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool cut = band_cuts(q0, kTile, k0, kTile, wl, wr);
-      const int key = k0 + r;
-#pragma unroll 1
-      for (int c = 0; c < kTile / 32; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + c * 32, sr);
-        tmem_ld32(tdP + lane_off + c * 32, dr);
-        tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-        const bool plain = !cut && !kAlibi;
-#pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[c * 32 + t]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[c * 32 + t]);
-          const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = c * 32 + t + e;  // query index within the tile
-            float z = fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]);
-            float pe;
-            if (plain) {
-              pe = ex2_approx(z);
-            } else {
-              if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - q0 - col)), z);
-              pe = ex2_approx(z);
-              if (cut && !band_visible(q0 + col, key, wl, wr)) pe = 0.f;
-            }
-            pv[e] = pe;
-            dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
-          }
-          pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
-          pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
-          dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
-          dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
-        }
-        // P^T over columns already read: [16c, 16c + 16) <= [32c, 32c + 32)
-        tmem_st16(tS + lane_off + c * 16, pk);
-        store_row_chunk_sw128(s.dst, r, c, dk);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&s.p_full);
-
-      if (kAtomicDq) {
-        if (!warp_wait(&s.mma_done, it & 1, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int qrow = q0 + r;  // dQ tile rows are queries
-        float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + qrow) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t g[32];
-          tmem_ld32(tdQ + lane_off + c * 32, g);
-          tmem_ld_wait();
-          if (qrow < p.N) {
-#pragma unroll
-            for (int t = 0; t < 32; t += 4)
-              red_add_v4(dst + c * 32 + t, __uint_as_float(g[t]), __uint_as_float(g[t + 1]),
-                         __uint_as_float(g[t + 2]), __uint_as_float(g[t + 3]));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&s.tmem_free);
-      }
-    }
-
-    // ---------------------------------------------------------- epilogue
-    // A key tile the block mask leaves unseen has dK = dV = 0.
-    bool done = ok;
-    if (ok && !kAtomicDq && n_it > 0)
-      done = warp_wait(&s.mma_done, (n_it - 1) & 1, p.err, abort_flag);
-    if (named_bar_and(1, 128, done)) {
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], b[32];
-        if (n_it > 0) {
-          tmem_ld32(tdV + lane_off + c * 32, a);
-          tmem_ld32(tdK + lane_off + c * 32, b);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
-        }
-        uint32_t pa[16], pb[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          pa[t] = pack2<kBf16>(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
-          pb[t] = pack2<kBf16>(__uint_as_float(b[2 * t]) * p.scale,
-                               __uint_as_float(b[2 * t + 1]) * p.scale);
-        }
-        store_row_chunk_sw128(s.dO, r, c, pa);
-        store_row_chunk_sw128(s.q, r, c, pb);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tid == 0) {
-        for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-          tma_store_4d(&p.map_dv, s.dO + kb * Smem::kBlockBytes, kb * 64, k0, hh, bb);
-          tma_store_4d(&p.map_dk, s.q + kb * Smem::kBlockBytes, kb * 64, k0, hh, bb);
-        }
-        tma_store_commit();
-        tma_store_wait_all();
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 4) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// dK / dV for D = 128, software-pipelined over 64-row query tiles
+// dK / dV, software-pipelined over 64-row query tiles (D = 64 or 128)
 // ---------------------------------------------------------------------------
 // With 64-row query tiles the scores and their gradient take 64 TMEM columns
 // each, so two tiles' S^T / dP^T fit beside the dV and dK accumulators:
@@ -441,17 +137,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 // shared memory, which bounds them at 48 cycles per 128 x 64 x 16 product.
 // dQ is formed transposed, dQ^T = K^T dS^T (M = D), so TMEM lane = column d
 // and each atomic warp instruction covers 32 consecutive floats of one dQ row.
-constexpr int kD128Threads = 480;  // warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA
+// At D = 64 the dQ^T product still runs with M = 128: output row m depends
+// only on A row m, so rows 64..127 (read past K's tile in shared memory) are
+// computed and never drained.
+constexpr int kPipeThreads = 480;  // warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA
 constexpr int kQ64 = 64;
 
-template <bool kSparse>
-struct Dkdv128Smem {
+template <int D, bool kSparse>
+struct DkdvPipeSmem {
+  static constexpr int kDBlocks = D / 64;      // 64-column blocks of a row
   static constexpr int kKBlock = kTile * 128;  // 128 rows x 128 B
   static constexpr int kQBlock = kQ64 * 128;   // 64 rows x 128 B
-  alignas(1024) uint8_t k[2 * kKBlock];        // [D block][128 keys][64 d]
-  alignas(1024) uint8_t v[2 * kKBlock];
-  alignas(1024) uint8_t q[3][2 * kQBlock];     // [stage][D block][64 queries][64 d]
-  alignas(1024) uint8_t dO[3][2 * kQBlock];
+  alignas(1024) uint8_t k[kDBlocks * kKBlock];     // [D block][128 keys][64 d]
+  alignas(1024) uint8_t v[kDBlocks * kKBlock];
+  alignas(1024) uint8_t q[3][kDBlocks * kQBlock];  // [stage][D block][64 queries][64 d]
+  alignas(1024) uint8_t dO[3][kDBlocks * kQBlock];
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
@@ -463,11 +163,11 @@ struct Dkdv128Smem {
   uint32_t q_tiles[kSparse ? 2 * kMaxSparseTiles / 32 : 1];  // block-sparse: 64-row query tiles
 };
 
-template <bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
-__global__ void __launch_bounds__(kD128Threads, 1)
-    bwd_dkdv_d128_kernel(const __grid_constant__ BwdLaunch p) {
-  constexpr int D = 128;
-  using Smem = Dkdv128Smem<kSparse>;
+template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+    bwd_dkdv_pipe_kernel(const __grid_constant__ BwdLaunch p) {
+  using Smem = DkdvPipeSmem<D, kSparse>;
+  constexpr int kDB = Smem::kDBlocks;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -528,8 +228,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
   if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&s.kv_full, 4 * Smem::kKBlock);
-      for (int kb = 0; kb < 2; ++kb) {
+      mbar_arrive_expect_tx(&s.kv_full, 2 * kDB * Smem::kKBlock);
+      for (int kb = 0; kb < kDB; ++kb) {
         tma_load_4d(s.k + kb * Smem::kKBlock, &p.map_k, &s.kv_full, kb * 64, k0, hh, bb);
         tma_load_4d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
       }
@@ -538,8 +238,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         const int st = it % 3;
         if (it >= 3 && !mbar_wait(&s.qdo_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
         const int q0 = qt * kQ64;
-        mbar_arrive_expect_tx(&s.qdo_full[st], 4 * Smem::kQBlock + 2 * kQ64 * 4);
-        for (int kb = 0; kb < 2; ++kb) {
+        mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
+        for (int kb = 0; kb < kDB; ++kb) {
           tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, hh, bb);
           tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0, hh, bb);
         }
@@ -592,7 +292,8 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     // ------------------------------------------------------------ gradient products
     if (lane == 0) {
       constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
-      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);  // d x queries, over keys
+      // d x queries, over keys; M = 128 at D = 64 too (rows past D unused)
+      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
       const uint32_t k_addr = smem_u32(s.k);
       bool ok = true;
       // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) & 1.
@@ -703,7 +404,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
         const int q0 = qt_dq * kQ64;
         qt_dq = walk.next(qt_dq);
         float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
-        const int nq = min(kQ64, p.N - q0);
+        const int nq = d < D ? min(kQ64, p.N - q0) : 0;  // lanes past D hold no dQ
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -821,11 +522,12 @@ __global__ void __launch_bounds__(kD128Threads, 1)
     const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
     if (named_bar_and(1, 256, done)) {
       tc_fence_after();
-      uint8_t* dk_tile = s.q[0];   // 32 KB of the free query ring
+      // D x 128 keys x 2 B of the free query ring each (16 or 32 KB of 24 or 48)
+      uint8_t* dk_tile = s.q[0];
       uint8_t* dv_tile = s.dO[0];
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {  // this warp's 64 d columns, 32 at a time
-        const int c32 = half * 2 + c;
+      for (int c = 0; c < kDB; ++c) {  // this warp's D / 2 columns, 32 at a time
+        const int c32 = half * kDB + c;
         uint32_t a[32], g[32];
         if (n_it > 0) {
           tmem_ld32(tdV + lane_off + c32 * 32, a);
@@ -848,7 +550,7 @@ __global__ void __launch_bounds__(kD128Threads, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
       if (tid == 0) {
-        for (int kb = 0; kb < 2; ++kb) {
+        for (int kb = 0; kb < kDB; ++kb) {
           tma_store_4d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
           tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
         }
@@ -1164,19 +866,6 @@ cudaError_t set_smem(K kern, int bytes, bool& configured) {
   return e;
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
-cudaError_t launch_dkdv_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
-  const int smem = static_cast<int>(sizeof(DkdvSmem<D, kSparse>)) + 1024;
-  static bool configured = false;
-  cudaError_t e = set_smem(kern, smem, configured);
-  if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
-  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
-  return cudaGetLastError();
-}
-
 template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   auto kern = bwd_dq_kernel<D, kBf16, kAlibi, kSparse>;
@@ -1190,16 +879,16 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
-cudaError_t launch_dkdv128_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_d128_kernel<kBf16, kAlibi, kAtomic, kSparse>;
-  const int smem = static_cast<int>(sizeof(Dkdv128Smem<kSparse>)) + 1024;
+template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
+cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
+  auto kern = bwd_dkdv_pipe_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
+  const int smem = static_cast<int>(sizeof(DkdvPipeSmem<D, kSparse>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kD128Threads, smem, st>>>(a);
+  kern<<<static_cast<unsigned>(grid), kPipeThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -1207,18 +896,11 @@ template <int D, bool kBf16, bool kSparse>
 cudaError_t launch_dkdv_ds(const BwdLaunch& a, cudaStream_t st) {
   const bool atomic = a.dq_accum != nullptr;
   const bool alibi = a.band.alibi != nullptr;
-  if (D == 128) {
-    if (alibi)
-      return atomic ? launch_dkdv128_t<kBf16, true, true, kSparse>(a, st)
-                    : launch_dkdv128_t<kBf16, true, false, kSparse>(a, st);
-    return atomic ? launch_dkdv128_t<kBf16, false, true, kSparse>(a, st)
-                  : launch_dkdv128_t<kBf16, false, false, kSparse>(a, st);
-  }
   if (alibi)
-    return atomic ? launch_dkdv_t<D, kBf16, true, true, kSparse>(a, st)
-                  : launch_dkdv_t<D, kBf16, true, false, kSparse>(a, st);
-  return atomic ? launch_dkdv_t<D, kBf16, false, true, kSparse>(a, st)
-                : launch_dkdv_t<D, kBf16, false, false, kSparse>(a, st);
+    return atomic ? launch_dkdv_pipe_t<D, kBf16, true, true, kSparse>(a, st)
+                  : launch_dkdv_pipe_t<D, kBf16, true, false, kSparse>(a, st);
+  return atomic ? launch_dkdv_pipe_t<D, kBf16, false, true, kSparse>(a, st)
+                : launch_dkdv_pipe_t<D, kBf16, false, false, kSparse>(a, st);
 }
 
 template <int D, bool kBf16>
