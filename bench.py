@@ -669,8 +669,11 @@ def run_ours(args, w):
             "config": {"workload": f"{w.describe()} fwd+bwd "
                                    f"({'deterministic two-pass dQ' if det else 'atomic dQ'})",
                        "B": B, "H": H, "N": N, "D": D, "causal": w.causal,
-                       "l2": "inputs larger than L2 (each input tensor "
-                             f"{B * H * N * D * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                       "l2": (f"inputs larger than L2 (each input tensor "
+                              f"{B * H * N * D * 2 / 1e6:.0f} MB > 129 MB), no flush"
+                              if B * H * N * D * 2 > 129e6 else
+                              f"inputs fit in L2 (each input tensor "
+                              f"{B * H * N * D * 2 / 1e6:.0f} MB), no flush: a warm-L2 figure"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "frac_of_peak": {"fwd+bwd": value / world / peak_sust, "fwd": fwd_tf / peak_sust,
