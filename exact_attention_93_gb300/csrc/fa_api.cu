@@ -141,7 +141,8 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
   if (!tile_map(&a->map_q, q, s, dtype, L.q) || !tile_map(&a->map_k, k, s, dtype, L.k) ||
       !tile_map(&a->map_v, v, s, dtype, L.v) || !tile_map(&a->map_do, dO, s, dtype, L.dO) ||
       !tile_map(&a->map_q64, q, s, dtype, L.q, 64) ||
-      !tile_map(&a->map_do64, dO, s, dtype, L.dO, 64))
+      !tile_map(&a->map_do64, dO, s, dtype, L.dO, 64) ||
+      !tile_map(&a->map_k64, k, s, dtype, L.k, 64) || !tile_map(&a->map_v64, v, s, dtype, L.v, 64))
     return FA_ERR_CUDA;
   if (dq && !tile_map(&a->map_dq, dq, s, dtype, L.dq)) return FA_ERR_CUDA;
   if (dk && !tile_map(&a->map_dk, dk, s, dtype, L.dk)) return FA_ERR_CUDA;

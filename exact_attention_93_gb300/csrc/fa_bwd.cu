@@ -29,7 +29,6 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;  // deterministic dQ kernel
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
@@ -569,65 +568,90 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// deterministic dQ
+// deterministic dQ, software-pipelined over 64-key tiles (D = 64 or 128)
 // ---------------------------------------------------------------------------
+// One CTA per 128-row query tile.  dQ accumulates in TMEM over the key tiles
+// in a fixed order, so the result does not depend on scheduling:
+//   TMEM [128b, 128b + 64)       buffer b: S of key tile i (b = i & 1)
+//   TMEM [128b + 64, 128b + 128) buffer b: dP of tile i, then dS packed over
+//                                each elementwise warp's own 32 columns
+//   TMEM [256, 256 + D)          dQ
+// The score warp issues S = Q K^T and dP = dO V^T of tile i once buffer
+// i & 1 is free (dQ(i - 2), the last reader of its dS, done; K, V(i)
+// landed, confirmed by a relay warp so the issuing thread waits once per
+// tile); eight warps form dS = P (dP - Di), P = 2^(S * scale * log2 e -
+// LSE2), one query row per thread so its LSE and Di sit in registers; the
+// gradient warp issues dQ += dS K with dS read from TMEM.  Q and dO are
+// loaded once; K and V come through a three-stage ring.
+constexpr int kDqPipeThreads = 384;  // warps 0-7 elementwise, 8 relay, 9 producer, 10-11 MMA
+constexpr int kK64 = 64;
+
 template <int D, bool kSparse>
-struct DqSmem {
-  static constexpr int kBlocks = D / 64;
-  static constexpr int kBlockBytes = kTile * 128;
-  static constexpr int kTileBytes = kBlocks * kBlockBytes;
-  alignas(1024) uint8_t q[kTileBytes];  // reused for the dQ output tile
-  alignas(1024) uint8_t dO[kTileBytes];
-  alignas(1024) uint8_t k[kTileBytes];
-  alignas(1024) uint8_t v[kTileBytes];
-  alignas(1024) uint8_t ds[2 * kBlockBytes];  // dS: 128 queries x 128 keys
-  uint64_t qdo_full, k_full, k_empty, v_full, v_empty, s_full, p_full, mma_done, drain;
+struct DqPipeSmem {
+  static constexpr int kDBlocks = D / 64;
+  static constexpr int kQBlock = kTile * 128;  // 128 rows x 128 B
+  static constexpr int kKBlock = kK64 * 128;   // 64 rows x 128 B
+  alignas(1024) uint8_t q[kDBlocks * kQBlock];  // [D block][128 queries][64 d]; then dQ
+  alignas(1024) uint8_t dO[kDBlocks * kQBlock];
+  alignas(1024) uint8_t k[3][kDBlocks * kKBlock];  // [stage][D block][64 keys][64 d]
+  alignas(1024) uint8_t v[3][kDBlocks * kKBlock];
+  alignas(16) float lse2[kTile];
+  alignas(16) float di[kTile];
+  uint64_t q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], buf_ready[2];
+  uint64_t all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
-  uint32_t k_tiles[kSparse ? kMaxSparseTiles / 32 : 1];  // block-sparse: key tiles
+  uint32_t k_tiles[kSparse ? 2 * kMaxSparseTiles / 32 : 1];  // block-sparse: 64-key tiles
 };
 
 template <int D, bool kBf16, bool kAlibi, bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdLaunch p) {
-  using Smem = DqSmem<D, kSparse>;
+__global__ void __launch_bounds__(kDqPipeThreads, 1)
+    bwd_dq_pipe_kernel(const __grid_constant__ BwdLaunch p) {
+  using Smem = DqPipeSmem<D, kSparse>;
+  constexpr int kDB = Smem::kDBlocks;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (p.N + kTile - 1) / kTile;
-  const int Npad = n_tiles * kTile;
+  const int n_qt = (p.N + kTile - 1) / kTile;
+  const int Npad = n_qt * kTile;
+  const int n_k64 = (p.N + kK64 - 1) / kK64;
   // Head-major; when keys are bounded on the right only (causal) later
   // query tiles see more keys and go first.
-  const int bh = static_cast<int>(blockIdx.x / n_tiles);
+  const int bh = static_cast<int>(blockIdx.x / n_qt);
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int wl = p.band.win_left, wr = p.band.win_right;
-  const int qt = (wl < 0 && wr >= 0) ? n_tiles - 1 - static_cast<int>(blockIdx.x % n_tiles)
-                                     : static_cast<int>(blockIdx.x % n_tiles);
+  const int qt = (wl < 0 && wr >= 0) ? n_qt - 1 - static_cast<int>(blockIdx.x % n_qt)
+                                     : static_cast<int>(blockIdx.x % n_qt);
   const int q0 = qt * kTile;
-  int j_first, j_last;  // key tiles this query tile's band reaches
-  band_key_tiles(q0, kTile, kTile, n_tiles, wl, wr, j_first, j_last);
-  const TileWalk<kSparse> walk{j_first, j_last, n_tiles, TileSet{s.k_tiles, n_tiles}};
-  if constexpr (kSparse)
-    fill_tile_set(s.k_tiles, n_tiles, [&](int j) {
-      return j >= j_first && j <= j_last && block_kept(p.band, bh, p.H, n_tiles, qt, j);
+  int it_begin, it_last;  // 64-key tiles this query tile's band reaches
+  band_key_tiles(q0, kTile, kK64, n_k64, wl, wr, it_begin, it_last);
+  const TileWalk<kSparse> walk{it_begin, it_last, n_k64, TileSet{s.k_tiles, n_k64}};
+  if constexpr (kSparse)  // the mask's 128-key blocks hold 64-key tiles 2b, 2b + 1
+    fill_tile_set(s.k_tiles, n_k64, [&](int t) {
+      return t >= it_begin && t <= it_last && block_kept(p.band, bh, p.H, n_qt, qt, t >> 1);
     });
   __syncthreads();
-  const int n_kv = walk.count();
+  const int n_it = walk.count();
 
   if (tid == 0) {
-    mbar_init(&s.qdo_full, 1);
-    mbar_init(&s.k_full, 1);
-    mbar_init(&s.k_empty, 1);
-    mbar_init(&s.v_full, 1);
-    mbar_init(&s.v_empty, 1);
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.mma_done, 1);
-    mbar_init(&s.drain, 1);
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 256);
+      // the relay warp and the tcgen05.commit that retires dQ(it - 2)
+      mbar_init(&s.buf_ready[i], 2);
+      mbar_init(&s.drain[i], 1);
+    }
+    mbar_init(&s.all_done, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (warp == 9) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
   }
@@ -635,155 +659,185 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tS = tbase, tdP = tbase + 128, tdQ = tbase + 256;
+  const uint32_t tdQ = tbase + 256;
   volatile int* abort_flag = &s.abort_flag;
+  constexpr uint32_t ab = kBf16 ? 1u : 0u;
 
-  if (warp == 4) {
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&s.qdo_full, 2 * Smem::kTileBytes);
-      for (int kb = 0; kb < Smem::kBlocks; ++kb) {
-        tma_load_4d(s.q + kb * Smem::kBlockBytes, &p.map_q, &s.qdo_full, kb * 64, q0, hh, bb);
-        tma_load_4d(s.dO + kb * Smem::kBlockBytes, &p.map_do, &s.qdo_full, kb * 64, q0, hh, bb);
+      mbar_arrive_expect_tx(&s.q_full, 2 * kDB * Smem::kQBlock + 2 * kTile * 4);
+      for (int kb = 0; kb < kDB; ++kb) {
+        tma_load_4d(s.q + kb * Smem::kQBlock, &p.map_q, &s.q_full, kb * 64, q0, hh, bb);
+        tma_load_4d(s.dO + kb * Smem::kQBlock, &p.map_do, &s.q_full, kb * 64, q0, hh, bb);
       }
+      const long long off = static_cast<long long>(bh) * Npad + q0;
+      bulk_load(s.lse2, p.lse + off, kTile * 4, &s.q_full);
+      bulk_load(s.di, p.di + off, kTile * 4, &s.q_full);
       int issued = 0;
-      for (int j = 0, kt = walk.first(); j < n_kv; ++j, kt = walk.next(kt)) {
-        if (j >= 1 && !mbar_wait(&s.k_empty, (j - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(&s.k_full, Smem::kTileBytes);
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.k + kb * Smem::kBlockBytes, &p.map_k, &s.k_full, kb * 64, kt * kTile,
-                      hh, bb);
-        issued = 2 * j + 1;
-        if (j >= 1 && !mbar_wait(&s.v_empty, (j - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(&s.v_full, Smem::kTileBytes);
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.v + kb * Smem::kBlockBytes, &p.map_v, &s.v_full, kb * 64, kt * kTile,
-                      hh, bb);
-        issued = 2 * j + 2;
+      for (int it = 0, t = walk.first(); it < n_it; ++it, t = walk.next(t)) {
+        const int st = it % 3;
+        if (it >= 3 && !mbar_wait(&s.kv_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(&s.kv_full[st], 2 * kDB * Smem::kKBlock);
+        for (int kb = 0; kb < kDB; ++kb) {
+          tma_load_4d(s.k[st] + kb * Smem::kKBlock, &p.map_k64, &s.kv_full[st], kb * 64,
+                      t * kK64, hh, bb);
+          tma_load_4d(s.v[st] + kb * Smem::kKBlock, &p.map_v64, &s.kv_full[st], kb * 64,
+                      t * kK64, hh, bb);
+        }
+        issued = it + 1;
       }
       if (*abort_flag) {
+        // Let copies already in flight land before the CTA's smem goes away.
         int zero = 0;
-        mbar_wait(&s.qdo_full, 0, p.err, &zero, 100000000ull);
-        if (issued >= 1) mbar_wait(&s.k_full, ((issued - 1) >> 1) & 1, p.err, &zero, 100000000ull);
-        if (issued >= 2) mbar_wait(&s.v_full, ((issued - 2) >> 1) & 1, p.err, &zero, 100000000ull);
+        mbar_wait(&s.q_full, 0, p.err, &zero, 100000000ull);
+        for (int t = max(0, issued - 3); t < issued; ++t)
+          mbar_wait(&s.kv_full[t % 3], (t / 3) & 1, p.err, &zero, 100000000ull);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ relay
+    // Buffer it & 1 takes S, dP(it) once K, V(it) have landed (seen here)
+    // and dQ(it - 2) is done (its tcgen05.commit arrives on buf_ready).
+    for (int it = 0; it < n_it; ++it) {
+      if (!warp_wait(&s.kv_full[it % 3], (it / 3) & 1, p.err, abort_flag)) break;
+      if (lane == 0) {
+        mbar_arrive(&s.buf_ready[it & 1]);
+        if (it < 2) mbar_arrive(&s.buf_ready[it & 1]);  // no dQ(it - 2) to wait for
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ score products
     if (lane == 0) {
-      constexpr uint32_t ab = kBf16 ? 1u : 0u;
-      constexpr uint32_t idS = idesc_f16(128, 128, ab, 0, 0);
-      constexpr uint32_t idKM = idesc_f16(128, D, ab, 0, 1);
+      constexpr uint32_t idS = idesc_f16(128, kK64, ab, 0, 0);  // queries x keys, over d
       const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v), ds_addr = smem_u32(s.ds);
-      bool ok = mbar_wait(&s.qdo_full, 0, p.err, abort_flag);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (!mbar_wait(&s.k_full, j & 1, p.err, abort_flag)) break;
-        if (!mbar_wait(&s.v_full, j & 1, p.err, abort_flag)) break;
+      bool ok = mbar_wait(&s.q_full, 0, p.err, abort_flag);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int b = it & 1, st = it % 3;
+        if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
         tc_fence_after();
+        const uint32_t k_addr = smem_u32(s.k[st]), v_addr = smem_u32(s.v[st]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tS, desc_add(smem_desc_sw128(q_addr, 16, 1024), off),
-                    desc_add(smem_desc_sw128(k_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
+          const uint32_t oq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+          const uint32_t ok_ = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+          tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(q_addr, 16, 1024), oq),
+                    desc_add(smem_desc_sw128(k_addr, 16, 1024), ok_), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdP, desc_add(smem_desc_sw128(do_addr, 16, 1024), off),
-                    desc_add(smem_desc_sw128(v_addr, 16, 1024), off), idS, kk > 0 ? 1u : 0u);
+          const uint32_t oq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+          const uint32_t ok_ = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+          tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(do_addr, 16, 1024), oq),
+                    desc_add(smem_desc_sw128(v_addr, 16, 1024), ok_), idS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s.s_full);
-        tc_commit(&s.v_empty);
-        if (!mbar_wait(&s.p_full, j & 1, p.err, abort_flag)) break;
-        tc_fence_after();
-        // dQ += dS K : A = dS in smem K-major over keys, B = K MN-major
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          tc_mma_ss(tdQ, desc_add(smem_desc_sw128(ds_addr, 16, 1024), aoff),
-                    desc_add(smem_desc_sw128(k_addr, Smem::kBlockBytes, 1024), kk * 16 * 128), idKM,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&s.mma_done);
-        tc_commit(&s.k_empty);
+        tc_commit(&s.s_full[b]);
       }
-      tc_commit(&s.drain);
+      tc_commit(&s.drain[0]);
       int zero = 0;
-      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+      mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
     }
-  } else {
-    const int r = tid;  // query row within the tile
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ gradient products
+    if (lane == 0) {
+      constexpr uint32_t idQ = idesc_f16(128, D, ab, 0, 1);  // queries x d, over keys
+      for (int it = 0; it < n_it; ++it) {
+        const int b = it & 1, st = it % 3;
+        if (!mbar_wait(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(s.k[st]);
+        // dQ += dS K : A = dS packed in TMEM over the dP columns (keys 32h ..
+        // 32h + 31 in columns 32h .. 32h + 15), B = K MN-major (d contiguous)
+#pragma unroll
+        for (int kk = 0; kk < kK64 / 16; ++kk)
+          tc_mma_ts(tdQ, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                    desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&s.kv_empty[st]);  // S, dP(it) completed before dS(it) existed
+        tc_commit(&s.buf_ready[b]);  // frees buffer b for tile it + 2
+      }
+      // The score products all completed before the last dS existed, so
+      // this commit covers every product of the CTA.
+      tc_commit(&s.all_done);
+      tc_commit(&s.drain[1]);
+      int zero = 0;
+      mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ elementwise
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, key-column half
+    const int r = quad * 32 + lane;                // query row (TMEM lane)
     const int i = q0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    const long long srow = static_cast<long long>(bh) * Npad + i;
-    const float lse2 = p.lse[srow];
-    const float dii = p.di[srow];
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
-    bool ok = true;
-    for (int j = 0, kt = walk.first(); j < n_kv; ++j, kt = walk.next(kt)) {
-      if (!warp_wait(&s.s_full, j & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      if (j >= 1 && !warp_wait(&s.mma_done, (j - 1) & 1, p.err, abort_flag)) {
+    bool ok = warp_wait(&s.q_full, 0, p.err, abort_flag);
+    const float lse2 = s.lse2[r], dii = s.di[r];  // +inf / 0 for rows past N
+    for (int it = 0, t = walk.first(); ok && it < n_it; ++it, t = walk.next(t)) {
+      const int b = it & 1;
+      const int k0 = t * kK64;
+      if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int k0 = kt * kTile;
-      const bool cut = band_cuts(q0, kTile, k0, kTile, wl, wr);
-#pragma unroll 1
-      for (int c = 0; c < kTile / 32; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + c * 32, sr);
-        tmem_ld32(tdP + lane_off + c * 32, dr);
-        tmem_ld_wait();
-        uint32_t dk[16];
-        if (!cut && !kAlibi) {
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
+      tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
+      tmem_ld_wait();
+      const bool cut = band_cuts(q0, kTile, k0, kK64, wl, wr) || k0 + kK64 > p.N;
+      uint32_t dk[16];
+      if (!cut && !kAlibi) {
+        // two columns per packed instruction: -z = LSE2 - S * scale_log2,
+        // dS = P (dP - Di)
+        const uint64_t nsl2 = f32x2(-sl2, -sl2), l2 = f32x2(lse2, lse2);
+        const uint64_t neg1 = f32x2(-1.f, -1.f), d2 = f32x2(dii, dii);
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            float d2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float pe = ex2_approx(fmaf(__uint_as_float(sr[t + e]), sl2, -lse2));
-              d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
-            }
-            dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
-          }
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            float d2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = c * 32 + t + e;  // key index within the tile
-              float z = fmaf(__uint_as_float(sr[t + e]), sl2, -lse2);
-              if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(k0 + col - i)), z);
-              float pe = ex2_approx(z);
-              if (cut && !band_visible(i, k0 + col, wl, wr)) pe = 0.f;
-              d2[e] = pe * (__uint_as_float(dr[t + e]) - dii);
-            }
-            dk[t / 2] = pack2<kBf16>(d2[0], d2[1]);
-          }
+        for (int e = 0; e < 32; e += 2) {
+          const float2 nz = split_f32x2(
+              fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, l2));
+          const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
+          const uint64_t dd =
+              fma_f32x2(d2, neg1, f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])));
+          const float2 ds = split_f32x2(mul_f32x2(f32x2(p0, p1), dd));
+          dk[e / 2] = pack2<kBf16>(ds.x, ds.y);
         }
-        store_row_chunk_sw128(s.ds, r, c, dk);
+      } else {
+        // a tile the band cuts, a ragged last tile, or an ALiBi bias
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float d2v[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = k0 + half * 32 + e + u;
+            float z = fmaf(__uint_as_float(sr[e + u]), sl2, -lse2);
+            if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - i)), z);
+            float pe = ex2_approx(z);
+            if (key >= p.N || (cut && !band_visible(i, key, wl, wr))) pe = 0.f;
+            d2v[u] = pe * (__uint_as_float(dr[e + u]) - dii);
+          }
+          dk[e / 2] = pack2<kBf16>(d2v[0], d2v[1]);
+        }
       }
-      fence_proxy_async_smem();
+      // dS over the first 16 of this warp's own 32 dP columns (already read)
+      tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, dk);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      mbar_arrive(&s.p_full[b]);
     }
-    // A query tile the block mask leaves without keys has dQ = 0; its Q
-    // tile, the output stage, must have landed before it is overwritten.
-    const bool mine =
-        ok && (n_kv > 0 ? warp_wait(&s.mma_done, (n_kv - 1) & 1, p.err, abort_flag)
-                        : warp_wait(&s.qdo_full, 0, p.err, abort_flag));
-    if (named_bar_and(1, 128, mine)) {
+
+    // ---------------------------------------------------------- epilogue
+    // A query tile the block mask leaves without keys has dQ = 0; Q, the
+    // output stage, has landed (q_full) and no product reads it any more.
+    const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
+    if (named_bar_and(1, 256, done)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kDB; ++c) {  // this warp's D / 2 columns, 32 at a time
+        const int c32 = half * kDB + c;
         uint32_t g[32];
-        if (n_kv > 0) {
-          tmem_ld32(tdQ + lane_off + c * 32, g);
+        if (n_it > 0) {
+          tmem_ld32(tdQ + lane_off + c32 * 32, g);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -791,16 +845,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          pk[t] = pack2<kBf16>(__uint_as_float(g[2 * t]) * p.scale,
-                               __uint_as_float(g[2 * t + 1]) * p.scale);
-        store_row_chunk_sw128(s.q, r, c, pk);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack2<kBf16>(__uint_as_float(g[2 * e]) * p.scale,
+                               __uint_as_float(g[2 * e + 1]) * p.scale);
+        store_row_chunk_sw128(s.q, r, c32, pk);
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (tid == 0) {
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_store_4d(&p.map_dq, s.q + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
+        for (int kb = 0; kb < kDB; ++kb)
+          tma_store_4d(&p.map_dq, s.q + kb * Smem::kQBlock, kb * 64, q0, hh, bb);
         tma_store_commit();
         tma_store_wait_all();
       }
@@ -809,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -868,14 +922,14 @@ cudaError_t set_smem(K kern, int bytes, bool& configured) {
 
 template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dq_kernel<D, kBf16, kAlibi, kSparse>;
-  const int smem = static_cast<int>(sizeof(DqSmem<D, kSparse>)) + 1024;
+  auto kern = bwd_dq_pipe_kernel<D, kBf16, kAlibi, kSparse>;
+  const int smem = static_cast<int>(sizeof(DqPipeSmem<D, kSparse>)) + 1024;
   static bool configured = false;
   cudaError_t e = set_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  kern<<<static_cast<unsigned>(grid), kDqPipeThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ struct BwdLaunch {
   CUtensorMap map_q, map_k, map_v, map_do;  // box 64 x 128 x 1 x 1
   CUtensorMap map_dq, map_dk, map_dv;       // outputs, same geometry
   CUtensorMap map_q64, map_do64;            // Q and dO again, box 64 x 64 x 1 x 1
+  CUtensorMap map_k64, map_v64;             // K and V again, box 64 x 64 x 1 x 1
   const float* lse;                         // [BH][Npad] LSE * log2(e), +inf padding
   const float* di;                          // [BH][Npad] rowsum(dO * O), 0 padding
   float* dq_accum;                          // [BH][N][D] or nullptr

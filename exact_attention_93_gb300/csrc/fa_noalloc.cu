@@ -90,7 +90,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
       !tile_map(&a.map_dq, dq, B, H, N, D, dtype) || !tile_map(&a.map_dk, dk, B, H, N, D, dtype) ||
       !tile_map(&a.map_dv, dv, B, H, N, D, dtype) ||
       !tile_map(&a.map_q64, q, B, H, N, D, dtype, 64) ||
-      !tile_map(&a.map_do64, dO, B, H, N, D, dtype, 64))
+      !tile_map(&a.map_do64, dO, B, H, N, D, dtype, 64) ||
+      !tile_map(&a.map_k64, k, B, H, N, D, dtype, 64) ||
+      !tile_map(&a.map_v64, v, B, H, N, D, dtype, 64))
     return FA_ERR_CUDA;
   float* lse2 = reinterpret_cast<float*>(scratch);
   float* di = reinterpret_cast<float*>(scratch + di_off);
