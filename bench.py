@@ -483,6 +483,102 @@ def run_fp8_only(args, w):
           flush=True)
 
 
+def measure_e2e(args, w, inputs, dev, det, dist, world, flops):
+    """The step end to end through the same C-ABI calls, from pinned host
+    memory to pinned host memory.  Every step copies its four inputs in and
+    its five results (O, LSE, dQ, dK, dV) out inside the timed region; the
+    copies run on their own streams, double-buffered, so step k + 1's inputs
+    travel while step k computes and step k - 1's results travel back, as a
+    prefetching training loop would run them."""
+    import torch
+
+    from exact_attention_93_gb300 import fattn
+
+    B, H, N, D = w.B, w.H, w.N, w.D
+    pin = {k: v.pin_memory() for k, v in inputs.items()}
+    sets = []
+    for _ in range(2):
+        g = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in inputs.items()}
+        sets.append({
+            "g": g, "o": torch.empty_like(g["q"]),
+            "lse": torch.empty(B, H, N, dtype=torch.float32, device=dev),
+            "dq": torch.empty_like(g["q"]), "dk": torch.empty_like(g["q"]),
+            "dv": torch.empty_like(g["q"]),
+            "ws": fattn.alloc_workspace(B, H, N, D, det, dev)})
+    out_names = ("o", "lse", "dq", "dk", "dv")
+    host_out = [{k: torch.empty(sets[0][k].shape, dtype=sets[0][k].dtype, pin_memory=True)
+                 for k in out_names} for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "comp", "out")}
+
+    def compute(S):
+        g = S["g"]
+        fattn.fa_fwd(g["q"], g["k"], g["v"], S["o"], S["lse"], w.scale, w.causal)
+        fattn.fa_bwd(g["q"], g["k"], g["v"], S["o"], S["lse"], g["do"], S["dq"], S["dk"],
+                     S["dv"], w.scale, w.causal, det, S["ws"])
+
+    def run(steps, start=None, end=None):
+        if start is not None:
+            start.record(s_in)
+        for k in range(steps):
+            b = k % 2
+            S = sets[b]
+            if k >= 2:
+                s_in.wait_event(ev["comp"][b])  # step k - 2 no longer reads set b's inputs
+            with torch.cuda.stream(s_in):
+                for name in pin:
+                    S["g"][name].copy_(pin[name], non_blocking=True)
+                ev["in"][b].record(s_in)
+            s_comp.wait_event(ev["in"][b])
+            if k >= 2:
+                s_comp.wait_event(ev["out"][b])  # step k - 2's results have left set b
+            with torch.cuda.stream(s_comp):
+                compute(S)
+                ev["comp"][b].record(s_comp)
+            s_out.wait_event(ev["comp"][b])
+            with torch.cuda.stream(s_out):
+                for name in out_names:
+                    host_out[b][name].copy_(S[name], non_blocking=True)
+                ev["out"][b].record(s_out)
+        if end is not None:
+            end.record(s_out)
+
+    run(2)
+    torch.cuda.synchronize()
+    if fattn.fa_device_error() != fattn.FA_OK:
+        raise RuntimeError("a kernel reported a timed-out wait in the end-to-end runs")
+    if dist is not None:
+        dist.barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(args.steps, s2, e2)
+    torch.cuda.synchronize()
+    e_ms = slowest_rank(s2.elapsed_time(e2) / args.steps, dist, dev)
+
+    # the copies alone, for context (outside the timed region)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s_in):
+        t0.record(s_in)
+        for name in pin:
+            sets[0]["g"][name].copy_(pin[name], non_blocking=True)
+        t1.record(s_in)
+    torch.cuda.synchronize()
+    h2d_ms = t0.elapsed_time(t1)
+    with torch.cuda.stream(s_out):
+        t0.record(s_out)
+        for name in out_names:
+            host_out[0][name].copy_(sets[0][name], non_blocking=True)
+        t1.record(s_out)
+    torch.cuda.synchronize()
+    d2h_ms = t0.elapsed_time(t1)
+    return {"value": whole_job_tflops(world, flops, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbps_alone": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbps_alone": d2h / (d2h_ms * 1e-3) / 1e9,
+            "pipeline": "copies on their own streams, double-buffered: step k+1's inputs and step "
+                        "k-1's results travel while step k computes"}
+
+
 def run_ours(args, w):
     import torch
 
@@ -587,34 +683,7 @@ def run_ours(args, w):
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H results
     e2e = None
     if not args.no_e2e:
-        pin = {k: v.pin_memory() for k, v in inputs.items()}
-        outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
-        h2d = sum(v.numel() * v.element_size() for v in pin.values())
-        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-
-        def e2e_step():
-            for k2 in pin:
-                g[k2].copy_(pin[k2], non_blocking=True)
-            step()
-            for k2 in outs:
-                host_out[k2].copy_(outs[k2], non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e2.record(stream)
-        torch.cuda.synchronize()
-        e_ms = s2.elapsed_time(e2) / args.steps
-        e_ms = slowest_rank(e_ms, dist, dev)
-        e2e = {"value": whole_job_tflops(world, fwd_f + bwd_alg, e_ms), "unit": "TFLOP/s",
-               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        e2e = measure_e2e(args, w, inputs, dev, det, dist, world, fwd_f + bwd_alg)
 
     # the long-context forward-only workload, reported beside the step
     extra = {}
