@@ -912,20 +912,12 @@ __global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
   mbar_wait(&bar, 0, err, &abort_flag, limit_ns);
 }
 
-template <typename K>
-cudaError_t set_smem(K kern, int bytes, bool& configured) {
-  if (configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) configured = true;
-  return e;
-}
-
 template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   auto kern = bwd_dq_pipe_kernel<D, kBf16, kAlibi, kSparse>;
   const int smem = static_cast<int>(sizeof(DqPipeSmem<D, kSparse>)) + 1024;
-  static bool configured = false;
-  cudaError_t e = set_smem(kern, smem, configured);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
@@ -937,8 +929,8 @@ template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
 cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
   auto kern = bwd_dkdv_pipe_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
   const int smem = static_cast<int>(sizeof(DkdvPipeSmem<D, kSparse>)) + 1024;
-  static bool configured = false;
-  cudaError_t e = set_smem(kern, smem, configured);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;

@@ -613,12 +613,9 @@ template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8 = false>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse, kFp8>;
   const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse, kFp8>)) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
+  if (e != cudaSuccess) return e;
   const long long n_q_tiles = (a.N + kTile - 1) / kTile;
   const long long grid = (n_q_tiles + 1) / 2 * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;

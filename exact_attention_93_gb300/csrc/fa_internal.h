@@ -5,9 +5,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace fa {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute belongs to the function as loaded
+// on each device, so a process that drives several GPUs sets it on each.
+// `done` is the calling launcher's own bitmask of devices already set
+// (devices past 63 are set on every call).
+template <typename K>
+cudaError_t ensure_dynamic_smem(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 

@@ -28,26 +28,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A [slices][rows][inner] tensor of 2- or 4-byte elements, rows `row_stride`
-// elements apart, slices `slice_stride` elements apart.  Boxes are
-// box_inner x box_rows x 1; out-of-range rows read as zero.
-// Returns false when the driver rejects the map (alignment, sizes).
-inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
-                         int elem_bytes, uint64_t inner, uint64_t rows, uint64_t slices,
-                         uint64_t row_stride, uint64_t slice_stride, uint32_t box_inner,
-                         uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {inner, rows, slices};
-  cuuint64_t strides[2] = {row_stride * elem_bytes, slice_stride * elem_bytes};
-  cuuint32_t box[3] = {box_inner, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // A [batch][head][rows][inner] tensor of elem_bytes-byte elements with
 // arbitrary element strides for rows, heads and batches (inner contiguous).
 // Boxes are box_inner x box_rows x 1 x 1; out-of-range rows (and inner

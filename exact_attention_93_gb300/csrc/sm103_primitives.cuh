@@ -113,48 +113,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-warpgroup register budgets (every thread of the warpgroup executes the
-// same instruction).  The budgets of all warpgroups must add up to no more
-// than the block was launched with.
-// ---------------------------------------------------------------------------
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
-// ---------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA stores and tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// ---------------------------------------------------------------------------
-// TMA (cp.async.bulk.tensor), 3-D tiled, completion counted in bytes on an
-// mbarrier.  Coordinates are {inner (elements), row, slice}.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
 }
 
 // 4-D tiled forms, coordinates {inner (elements), row, head, batch}.
