@@ -121,6 +121,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// TMA (bulk tensor copies)
+// ---------------------------------------------------------------------------
 // 4-D tiled forms, coordinates {inner (elements), row, head, batch}.
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, uint64_t* bar,
                                             int c0, int c1, int c2, int c3) {
