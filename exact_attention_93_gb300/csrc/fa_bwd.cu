@@ -443,13 +443,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         if (lane == 0) mbar_arrive(&s.s_read[b]);
       }
       const bool cut = band_cuts(q0, kQ64, k0, kTile, wl, wr);
+      // ALiBi on a tile wholly on one side of the diagonal: |key - q| is
+      // linear in the column, the bias B + D e (e = column of this half)
+      const bool below = k0 + kTile - 1 <= q0, above = q0 + kQ64 - 1 <= k0;
+      const bool lin = kAlibi && (below || above);
       uint32_t pk[16], dk[16];
-      if (!cut && !kAlibi) {
-        // P = 2^(S * scale * log2 e - LSE2) and dS = P (dP - Di), two
-        // columns per packed instruction: the elementwise warps share
+      if (!cut && (!kAlibi || lin)) {
+        // P = 2^(S * scale * log2 e - LSE2 [+ bias]) and dS = P (dP - Di),
+        // two columns per packed instruction: the elementwise warps share
         // their SM sub-partitions with the MMA-issuing warps, so every
         // instruction saved here is issue time given back to the tensor core.
         const uint64_t nsl2 = f32x2(-sl2, -sl2), neg1 = f32x2(-1.f, -1.f);
+        const float qk = static_cast<float>(q0 + half * 32 - (k0 + r));  // query - key at e = 0
+        const float sd = below ? nslope2 : -nslope2;
+        const uint64_t nb2 = f32x2(-sd * qk, -sd * qk), nd2 = f32x2(-sd, -sd);
 #pragma unroll
         for (int t = 0; t < 32; t += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
@@ -457,10 +464,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int e = t + 2 * h;
-            // -z = LSE2 - S * scale_log2
+            uint64_t l2 = h ? f32x2(l4.z, l4.w) : f32x2(l4.x, l4.y);
+            if (lin)  // LSE2 - bias
+              l2 = fma_f32x2(f32x2(static_cast<float>(e), static_cast<float>(e + 1)), nd2,
+                             add_f32x2(l2, nb2));
+            // -z = LSE2 [- bias] - S * scale_log2
             const float2 nz = split_f32x2(
-                fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2,
-                          h ? f32x2(l4.z, l4.w) : f32x2(l4.x, l4.y)));
+                fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, l2));
             const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
             const uint64_t dd =
                 fma_f32x2(h ? f32x2(d4.z, d4.w) : f32x2(d4.x, d4.y), neg1,
@@ -786,16 +796,27 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
       tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
       tmem_ld_wait();
       const bool cut = band_cuts(q0, kTile, k0, kK64, wl, wr) || k0 + kK64 > p.N;
+      // ALiBi on a tile wholly on one side of the diagonal: |key - i| is
+      // linear in the column, the bias B + D e (e = column of this half)
+      const bool below = k0 + kK64 - 1 <= q0, above = q0 + kTile - 1 <= k0;
+      const bool lin = kAlibi && (below || above);
       uint32_t dk[16];
-      if (!cut && !kAlibi) {
-        // two columns per packed instruction: -z = LSE2 - S * scale_log2,
-        // dS = P (dP - Di)
-        const uint64_t nsl2 = f32x2(-sl2, -sl2), l2 = f32x2(lse2, lse2);
+      if (!cut && (!kAlibi || lin)) {
+        // two columns per packed instruction: -z = LSE2 [- bias] -
+        // S * scale_log2, dS = P (dP - Di)
+        const uint64_t nsl2 = f32x2(-sl2, -sl2);
+        const float kq = static_cast<float>(k0 + half * 32 - i);  // key - query at e = 0
+        const float sd = above ? nslope2 : -nslope2;
+        const uint64_t lb2 = f32x2(lse2 - sd * kq, lse2 - sd * kq), nd2 = f32x2(-sd, -sd);
+        const uint64_t l2 = f32x2(lse2, lse2);
         const uint64_t neg1 = f32x2(-1.f, -1.f), d2 = f32x2(dii, dii);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
+          const uint64_t off =
+              lin ? fma_f32x2(f32x2(static_cast<float>(e), static_cast<float>(e + 1)), nd2, lb2)
+                  : l2;
           const float2 nz = split_f32x2(
-              fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, l2));
+              fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, off));
           const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
           const uint64_t dd =
               fma_f32x2(d2, neg1, f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])));

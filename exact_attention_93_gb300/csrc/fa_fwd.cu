@@ -455,9 +455,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       const bool prescale = kAlibi || !pos_scale;
       if (kAlibi) {
         const float d0 = static_cast<float>(k0 - i);  // key - query at column 0 (exact)
+        const bool below = k0 + kTile - 1 <= q0, above = k0 >= q0 + kTile - 1;
+        if (below || above) {
+          // The whole tile lies on one side of the diagonal: |key - i| is
+          // linear in the column, so the bias is B + D c, two columns per
+          // packed FMA.
+          const float sd = above ? nslope2 : -nslope2;
+          const uint64_t b2 = f32x2(sd * d0, sd * d0), dd2 = f32x2(sd, sd), s2 = f32x2(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          sv[c] = fmaf(sv[c], sl2, nslope2 * fabsf(d0 + static_cast<float>(c)));
+          for (int c = 0; c < kTile; c += 2) {
+            const uint64_t bias = fma_f32x2(f32x2(static_cast<float>(c), static_cast<float>(c + 1)),
+                                            dd2, b2);
+            const float2 x = split_f32x2(fma_f32x2(f32x2(sv[c], sv[c + 1]), s2, bias));
+            sv[c] = x.x;
+            sv[c + 1] = x.y;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTile; ++c)
+            sv[c] = fmaf(sv[c], sl2, nslope2 * fabsf(d0 + static_cast<float>(c)));
+        }
       } else if (!pos_scale) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c) sv[c] *= sl2;
