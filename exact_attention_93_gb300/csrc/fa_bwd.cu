@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
         }
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();
       }
     }
   }
@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
         for (int kb = 0; kb < kDB; ++kb)
           tma_store_4d(&p.map_dq, s.q + kb * Smem::kQBlock, kb * 64, q0, hh, bb);
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();
       }
     }
   }

@@ -148,8 +148,11 @@ __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+// Wait until every committed bulk store has read its shared-memory source:
+// the staging buffer may then be reused or the CTA may exit.  The global
+// writes themselves complete with the kernel.
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

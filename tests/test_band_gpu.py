@@ -87,6 +87,10 @@ ALIBI = [
     (2, 2, 200, 128, "bf16", True, (-1, -1), True),
     (1, 2, 400, 128, "bf16", False, (90, 40), False),
     (1, 2, 300, 64, "bf16", True, (64, -1), True),
+    # long rows: most tiles lie wholly on one side of the diagonal, where the
+    # kernels add the bias in its linear form, over distances up to N - 1
+    (1, 2, 2048, 64, "bf16", False, (-1, -1), False),
+    (1, 1, 1536, 128, "bf16", True, (-1, -1), False),
 ]
 
 
