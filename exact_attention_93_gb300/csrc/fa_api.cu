@@ -152,6 +152,14 @@ fa_status make_bwd_launch(BwdLaunch* a, const void* q, const void* k, const void
   a->lse = reinterpret_cast<const float*>(base + w.lse2);
   a->di = reinterpret_cast<const float*>(base + w.di);
   a->dq_accum = deterministic ? nullptr : reinterpret_cast<float*>(base + w.dq);
+  if (a->dq_accum && s.D == 64 &&
+      !make_tmap_4d(&a->map_dqacc, a->dq_accum, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.N),
+                    static_cast<uint64_t>(s.H), static_cast<uint64_t>(s.B),
+                    static_cast<uint64_t>(s.D), static_cast<uint64_t>(s.N) * s.D,
+                    static_cast<uint64_t>(s.H) * s.N * s.D, static_cast<uint32_t>(s.D), 64,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, 4))
+    return FA_ERR_CUDA;
   a->N = s.N;
   a->BH = static_cast<int>(s.BH());
   a->D = s.D;

@@ -154,9 +154,13 @@ struct DkdvPipeSmem {
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
   alignas(16) float lse2[3][kQ64];
   alignas(16) float di[3][kQ64];
+  // D = 64, atomic mode: drained dQ tiles [64 queries][D] for the bulk
+  // reductions, double-buffered
+  alignas(1024) float dq_stage[D == 64 ? 2 : 1][D == 64 ? kQ64 * D : 1];
   uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], s_read[2], p_full[2];
   uint64_t buf_ready[2];
   uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
+  uint64_t stage_full[2], stage_free[2];
   uint32_t tmem_base;
   int abort_flag;
   uint32_t q_tiles[kSparse ? 2 * kMaxSparseTiles / 32 : 1];  // block-sparse: 64-row query tiles
@@ -206,6 +210,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       mbar_init(&s.buf_ready[i], 5);
       mbar_init(&s.tmem_free[i], 128);
       mbar_init(&s.drain[i], 1);
+      mbar_init(&s.stage_full[i], 2);  // the two buffer warps holding dQ rows d < 64
+      mbar_init(&s.stage_free[i], 1);  // the thread that issues the reductions
     }
     mbar_init(&s.ds_last, 256);
     mbar_init(&s.all_done, 1);
@@ -402,16 +408,52 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       if (drain) {
         const int q0 = qt_dq * kQ64;
         qt_dq = walk.next(qt_dq);
-        float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
-        const int nq = d < D ? min(kQ64, p.N - q0) : 0;  // lanes past D hold no dQ
+        if constexpr (D == 64) {
+          // Stage the tile in shared memory ([query][d], rows d < 64 come
+          // from quadrants 0 and 1) and add it into the accumulator with one
+          // bulk tensor reduction instead of 64 atomics per thread; rows
+          // past N fall outside the tensor map and are dropped.
+          if (quad < 2) {
+            const int sb = j & 1;
+            if (j >= 2 && !warp_wait(&s.stage_free[sb], ((j >> 1) - 1) & 1, p.err, abort_flag))
+              break;
+            float* stage = s.dq_stage[sb];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (h * 32 + c < nq)
-              atomicAdd(dst + static_cast<long long>(h * 32 + c) * D, __uint_as_float(g[h][c]));
+              for (int c = 0; c < 32; ++c) stage[(h * 32 + c) * D + d] = __uint_as_float(g[h][c]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.stage_full[sb]);
+            if (warp == 8) {
+              bool issued = true;  // one lane issues; the warp leaves the loop together
+              if (lane == 0) {
+                issued = mbar_wait(&s.stage_full[sb], (j >> 1) & 1, p.err, abort_flag);
+                if (issued) {
+                  tma_reduce_add_4d(&p.map_dqacc, stage, 0, q0, hh, bb);
+                  tma_store_commit();
+                  // the reduction of tile j - 1 has read its buffer: free it
+                  tma_store_wait_read_all_but_newest();
+                  if (j >= 1) mbar_arrive(&s.stage_free[(j - 1) & 1]);
+                }
+              }
+              if (!__all_sync(0xffffffffu, issued)) break;
+            }
+          }
+        } else {
+          float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
+          const int nq = d < D ? min(kQ64, p.N - q0) : 0;  // lanes past D hold no dQ
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (h * 32 + c < nq)
+                atomicAdd(dst + static_cast<long long>(h * 32 + c) * D, __uint_as_float(g[h][c]));
+        }
       }
     }
+    // the last bulk reductions must have read shared memory before it goes
+    if (kAtomicDq && D == 64 && warp == 8 && lane == 0) tma_store_wait_all();
   } else {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, query-column half
@@ -564,7 +606,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
         }
         tma_store_commit();
-        tma_store_wait_read();
+        tma_store_wait_all();
       }
     }
   }
@@ -877,7 +919,7 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
         for (int kb = 0; kb < kDB; ++kb)
           tma_store_4d(&p.map_dq, s.q + kb * Smem::kQBlock, kb * 64, q0, hh, bb);
         tma_store_commit();
-        tma_store_wait_read();
+        tma_store_wait_all();
       }
     }
   }

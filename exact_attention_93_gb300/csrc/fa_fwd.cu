@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           for (int kb = 0; kb < Smem::kOBlocks; ++kb)
             tma_store_4d(&p.map_o, stage + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
           tma_store_commit();
-          tma_store_wait_read();
+          tma_store_wait_all();
         }
         if (i < p.N)
           p.lse[static_cast<long long>(bh) * p.N + i] =

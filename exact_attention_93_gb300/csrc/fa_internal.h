@@ -75,6 +75,9 @@ struct BwdLaunch {
   CUtensorMap map_dq, map_dk, map_dv;       // outputs, same geometry
   CUtensorMap map_q64, map_do64;            // Q and dO again, box 64 x 64 x 1 x 1
   CUtensorMap map_k64, map_v64;             // K and V again, box 64 x 64 x 1 x 1
+  // D = 64, atomic mode: dq_accum as fp32 {D, N, H, B}, box 64 x 64 x 1 x 1,
+  // no swizzle (the target of the dQ bulk reductions)
+  CUtensorMap map_dqacc;
   const float* lse;                         // [BH][Npad] LSE * log2(e), +inf padding
   const float* di;                          // [BH][Npad] rowsum(dO * O), 0 padding
   float* dq_accum;                          // [BH][N][D] or nullptr

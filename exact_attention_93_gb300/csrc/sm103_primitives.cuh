@@ -144,15 +144,32 @@ __device__ __forceinline__ void tma_store_4d(const void* tmap, const void* smem_
       : "memory");
 }
 
+// Bulk tensor reduction: add a shared-memory tile into global memory
+// (element-wise, atomic per element at L2), coordinates as tma_store_4d.
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, const void* smem_src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Wait until all committed bulk groups but the newest have read their
+// shared-memory sources.
+__device__ __forceinline__ void tma_store_wait_read_all_but_newest() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Wait until every committed bulk store has read its shared-memory source:
-// the staging buffer may then be reused or the CTA may exit.  The global
-// writes themselves complete with the kernel.
-__device__ __forceinline__ void tma_store_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Wait until every committed bulk store has completed.  (Waiting only for
+// the shared-memory reads, cp.async.bulk.wait_group.read, let CTAs exit
+// sooner but measured 3 % slower on the 8-bit forward.)
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
