@@ -709,6 +709,9 @@ def run_ours(args, w):
                                          "note": "back-to-back launches; inputs 16.8 MB each fit in L2"}
         extra.update(band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk))
         extra.update(fp8_extras(w, dev, stream, pk))
+        # head dimension 64 at the same sequence length and work (twice the heads)
+        extra.update(fp8_extras(W.custom(w.B, 2 * w.H, w.N, 64, causal=w.causal, seed=w.seed,
+                                         backward=False), dev, stream, pk))
         extra.update(small_config_extras(dev, stream, pk))
 
     cpu = None

@@ -168,7 +168,7 @@ def flash_attn_fp8_func(q, k, v, softmax_scale=None, causal=False, window_size=(
                         alibi_slopes=None, block_mask=None, descale_q=None, descale_k=None,
                         descale_v=None, return_lse=False):
     """Forward-only attention of e4m3 q, k, v (torch.float8_e4m3fn, shaped
-    (batch, seqlen, nheads, 128), head dim contiguous, other strides multiples
+    (batch, seqlen, nheads, 64 or 128), head dim contiguous, other strides multiples
     of 16).  descale_q / descale_k / descale_v: None or fp32 (batch, nheads)
     factors; the result is attention of descale_q * q, descale_k * k and
     descale_v * v, returned in bf16 (with the fp32 (batch, nheads, seqlen)

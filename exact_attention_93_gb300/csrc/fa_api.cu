@@ -252,9 +252,8 @@ fa_status fwd8_impl(const void* q, const void* k, const void* v, void* o, float*
                     const Shape& s, const Layout& L, const fa_options* opt,
                     const float* descale_q, const float* descale_k, const float* descale_v,
                     float scale, int causal, void* ws, size_t ws_bytes, void* stream) {
-  fa_status st = check_shape(s, FA_BF16);
+  fa_status st = check_shape(s, FA_BF16);  // D in {64, 128}
   if (st != FA_OK) return st;
-  if (s.D != 128) return FA_ERR_UNSUPPORTED;
   Band band;
   if ((st = make_band(opt, causal, s, &band)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -362,7 +361,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int D) {
   const Shape s{B, H, N, D};
-  if (check_shape(s, FA_BF16) != FA_OK || D != 128) return 0;
+  if (check_shape(s, FA_BF16) != FA_OK) return 0;
   return fwd8_ws_bytes(s);
 }
 

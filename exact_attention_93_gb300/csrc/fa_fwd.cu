@@ -62,17 +62,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D, bool kSparse, bool kFp8>
 struct FwdSmem {
-  static_assert(!kFp8 || D == 128, "8-bit operands: D = 128");
   static constexpr int kRowBytes = kFp8 ? D : 2 * D;  // one Q or K row
-  static constexpr int kBlocks = kRowBytes / 128;      // 128-byte column blocks
-  static constexpr int kBlockBytes = kTile * 128;      // 128 rows x 128 B
-  static constexpr int kTileBytes = kBlocks * kBlockBytes;
-  static constexpr int kOBlocks = D / 64;              // 16-bit O: 64-column blocks
+  // Q and K tiles: 128-byte column blocks (128-byte swizzle), or, for 8-bit
+  // D = 64, one block of 64-byte rows (64-byte swizzle)
+  static constexpr int kBlocks = kRowBytes >= 128 ? kRowBytes / 128 : 1;
+  static constexpr int kBlockBytes = kTile * (kRowBytes >= 128 ? 128 : kRowBytes);
+  static constexpr int kTileBytes = kBlocks * kBlockBytes;  // also V^T: D rows x 128 B
+  static constexpr int kOBlocks = D / 64;                   // 16-bit O: 64-column blocks
+  static constexpr int kOBlockBytes = kTile * 128;          // 128 rows x 128 B
   // tiles A and B; with 16-bit operands each is reused as its O staging
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[2][kTileBytes];
   alignas(1024) uint8_t v[2][kTileBytes];  // 8-bit: V^T, D rows x 128 keys
-  alignas(1024) uint8_t o[kFp8 ? 2 : 1][kFp8 ? kOBlocks * kBlockBytes : 16];
+  alignas(1024) uint8_t o[kFp8 ? 2 : 1][kFp8 ? kOBlocks * kOBlockBytes : 16];
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
@@ -143,6 +145,8 @@ template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
   using Smem = FwdSmem<D, kSparse, kFp8>;
   constexpr int kColsPerBlock = kFp8 ? 128 : 64;  // elements in a 128-byte block
+  // 8-bit D = 64: Q and K rows are 64 bytes, in 64-byte-swizzled tiles
+  constexpr bool kRows64 = Smem::kRowBytes < 128;
   // P = 2^(x - m + kPOffset) with the reference maximum m lagging the true
   // one by at most kThreshold, so P < 2^(kThreshold + kPOffset) = 256.
   // 16-bit P keeps the largest lag; 8-bit P (e4m3, largest finite 448,
@@ -277,8 +281,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
       constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, D) : idesc_f16(128, D, ab, 0, 1);
       // Operand descriptors are built once and advanced by constant offsets.
-      const uint64_t dq0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+      const uint64_t dq0 = kRows64 ? smem_desc_sw64(smem_u32(s.q[0]), 16, 512)
+                                   : smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
+      const uint64_t dk0 = kRows64 ? smem_desc_sw64(smem_u32(s.k[0]), 16, 512)
+                                   : smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t dv0 =
           smem_desc_sw128(smem_u32(s.v[0]), kFp8 ? 16 : Smem::kBlockBytes, 1024);
       // One product step covers 32 bytes of each row: 16 elements of 16 bits,
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             pk[e] = pack2<kBf16>(__uint_as_float(o[2 * e]) * inv_l,
                                  __uint_as_float(o[2 * e + 1]) * inv_l);
           // 32 columns = four 16-byte chunks of this row, 128-byte swizzle
-          uint8_t* blk = stage + (c >> 1) * Smem::kBlockBytes + r * 128;
+          uint8_t* blk = stage + (c >> 1) * Smem::kOBlockBytes + r * 128;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const int cc = (c & 1) * 4 + ch;
@@ -607,7 +613,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         named_bar_sync(1 + t, 128);
         if (r == 0) {
           for (int kb = 0; kb < Smem::kOBlocks; ++kb)
-            tma_store_4d(&p.map_o, stage + kb * Smem::kBlockBytes, kb * 64, q0, hh, bb);
+            tma_store_4d(&p.map_o, stage + kb * Smem::kOBlockBytes, kb * 64, q0, hh, bb);
           tma_store_commit();
           tma_store_wait_all();
         }
@@ -642,13 +648,14 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 
 // V^T for the 8-bit forward: the P V product wants its B operand K-major
 // (keys contiguous), so each (batch, head)'s [N, D] byte matrix is rewritten
-// as [D, ld] once per call.  A CTA moves one 128-key x 128-column tile; warp
-// w takes columns 16w .. 16w+15, lane l keys 4l .. 4l+3: four 16-byte row
-// loads, a 4 x 4 byte transpose per word (byte permutes) and sixteen 4-byte
-// stores, each warp-wide store covering 128 consecutive bytes of one V^T row.
+// as [D, ld] once per call.  A CTA (D / 16 warps) moves one 128-key x D-column
+// tile; warp w takes columns 16w .. 16w+15, lane l keys 4l .. 4l+3: four
+// 16-byte row loads, a 4 x 4 byte transpose per word (byte permutes) and
+// sixteen 4-byte stores, each warp-wide store covering 128 consecutive bytes
+// of one V^T row.
 __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __restrict__ v,
                                                            RowStrides sv, uint8_t* __restrict__ vt,
-                                                           int N, long long ld, int H,
+                                                           int N, long long ld, int H, int D,
                                                            int n_key_tiles) {
   const int bh = static_cast<int>(blockIdx.x / n_key_tiles);
   const int k0 = static_cast<int>(blockIdx.x % n_key_tiles) * kTile;
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __rest
   }
   const int kg = k0 + 4 * l;  // first key of this lane's group (a multiple of 4)
   if (kg >= ld) return;       // ld is a multiple of 16: the group lies wholly inside
-  uint8_t* dst = vt + static_cast<long long>(bh) * 128 * ld + kg;
+  uint8_t* dst = vt + static_cast<long long>(bh) * D * ld + kg;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {  // columns 16w + 4c .. 16w + 4c + 3
     const uint32_t w0 = (&row[0].x)[c], w1 = (&row[1].x)[c], w2 = (&row[2].x)[c],
@@ -684,13 +691,23 @@ __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __rest
 
 cudaError_t launch_transpose_v8(const void* v, RowStrides sv, void* vt, int N, long long ld, int H,
                                 long long BH, int D, cudaStream_t s) {
-  if (D != 128 || ld < N || (ld & 15) != 0) return cudaErrorInvalidValue;
+  if ((D != 64 && D != 128) || ld < N || (ld & 15) != 0) return cudaErrorInvalidValue;
   const long long tiles = (N + kTile - 1) / kTile;
   if (tiles * BH > INT_MAX) return cudaErrorInvalidConfiguration;
-  transpose_v8_kernel<<<static_cast<unsigned>(tiles * BH), 256, 0, s>>>(
-      static_cast<const uint8_t*>(v), sv, static_cast<uint8_t*>(vt), N, ld, H,
+  transpose_v8_kernel<<<static_cast<unsigned>(tiles * BH), D * 2, 0, s>>>(
+      static_cast<const uint8_t*>(v), sv, static_cast<uint8_t*>(vt), N, ld, H, D,
       static_cast<int>(tiles));
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd8_d(const FwdLaunch& a, cudaStream_t s) {
+  const bool alibi = a.band.alibi != nullptr, sparse = a.band.block_mask != nullptr;
+  if (sparse)
+    return alibi ? launch_fwd_t<D, true, true, true, true>(a, s)
+                 : launch_fwd_t<D, true, false, true, true>(a, s);
+  return alibi ? launch_fwd_t<D, true, true, false, true>(a, s)
+               : launch_fwd_t<D, true, false, false, true>(a, s);
 }
 
 template <int D, bool kBf16>
@@ -703,13 +720,8 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t s) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s) {
   if (a.fp8) {
-    if (a.D != 128 || !a.bf16) return cudaErrorInvalidValue;
-    const bool alibi = a.band.alibi != nullptr, sparse = a.band.block_mask != nullptr;
-    if (sparse)
-      return alibi ? launch_fwd_t<128, true, true, true, true>(a, s)
-                   : launch_fwd_t<128, true, false, true, true>(a, s);
-    return alibi ? launch_fwd_t<128, true, true, false, true>(a, s)
-                 : launch_fwd_t<128, true, false, false, true>(a, s);
+    if (!a.bf16) return cudaErrorInvalidValue;
+    return a.D == 64 ? launch_fwd8_d<64>(a, s) : launch_fwd8_d<128>(a, s);
   }
   if (a.D == 64) return a.bf16 ? launch_fwd_d<64, true>(a, s) : launch_fwd_d<64, false>(a, s);
   return a.bf16 ? launch_fwd_d<128, true>(a, s) : launch_fwd_d<128, false>(a, s);

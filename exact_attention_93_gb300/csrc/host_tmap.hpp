@@ -65,7 +65,8 @@ inline bool operand_map(CUtensorMap* map, const void* base, bool bf16, int B, in
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// An 8-bit [B, H, N, D] operand (D = 128: one 128-byte row per box row).
+// An 8-bit [B, H, N, D] operand, one whole row per box row: D = 128 with
+// 128-byte swizzle, D = 64 with 64-byte swizzle.
 inline bool operand_map_u8(CUtensorMap* map, const void* base, int B, int H, int N, int D,
                            long long batch_stride, long long head_stride, long long seq_stride,
                            int box_rows) {
@@ -73,7 +74,8 @@ inline bool operand_map_u8(CUtensorMap* map, const void* base, int B, int H, int
                       static_cast<uint64_t>(N), static_cast<uint64_t>(H),
                       static_cast<uint64_t>(B), static_cast<uint64_t>(seq_stride),
                       static_cast<uint64_t>(head_stride), static_cast<uint64_t>(batch_stride),
-                      128, static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B, 1);
+                      static_cast<uint32_t>(D), static_cast<uint32_t>(box_rows),
+                      D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, 1);
 }
 
 }  // namespace fa

@@ -338,6 +338,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle: rows of 64 bytes, 8-row
+// atoms of 512 bytes (what a TMA load with 64-byte swizzle and a 64-byte
+// inner box writes).  K-major: lbo unused (16), sbo = 512 (next 8 rows).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                                   uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  d |= 4ull << 61;  // 64-byte swizzle
+  return d;
+}
+
 // The same descriptor with its start moved by `bytes` (a multiple of 16).
 // The start field holds address >> 4 in 14 bits; shared-memory addresses stay
 // below 256 KB, so the addition never carries into the next field and a

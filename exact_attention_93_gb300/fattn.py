@@ -288,7 +288,7 @@ def alloc_fp8_workspace(B, H, N, D, device=None):
     torch = _torch()
     n = fa_fwd_fp8_workspace_size(B, H, N, D)
     if n == 0:
-        raise ValueError("invalid sizes for an FP8 forward (D must be 128)")
+        raise ValueError("invalid sizes for an FP8 forward (D must be 64 or 128)")
     buf = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
     off = (-buf.data_ptr()) % 256
     return buf[off:off + n]

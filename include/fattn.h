@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, bad scale   */
-  FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128} (FP8: not 128), unknown dtype  */
+  FA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, unknown dtype               */
   FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed              */
   FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait                */
 } fa_status;
@@ -163,8 +163,8 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 /*
  * Workspace bytes fa_fwd_fp8 needs: B*H*D*ld bytes (V transposed, ld = N
- * rounded up to 16), rounded up to 256.  Returns 0 for invalid sizes or
- * D != 128.
+ * rounded up to 16), rounded up to 256.  Returns 0 for invalid sizes
+ * (D not in {64, 128} included).
  */
 size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int D);
 
@@ -178,7 +178,7 @@ size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int D);
  *   o, lse = the fa_fwd_ex result for Q~, K~, V~   (o in bf16)
  *
  *   q, k, v     device, e4m3 bytes [B, H, N, D] in `layout` (strides in
- *               bytes, multiples of 16; NULL: contiguous).  D must be 128
+ *               bytes, multiples of 16; NULL: contiguous).  D is 64 or 128
  *               (FA_ERR_UNSUPPORTED otherwise).
  *   o           device, bf16 [B, H, N, D] in layout->o (elements, multiples
  *               of 8).   lse: device fp32 [B, H, N], natural log.

@@ -208,7 +208,7 @@ def test_block_mask_beyond_the_tile_limit_is_unsupported(lib):
 def fwd8(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=300, D=128, layout=None,
          opts=None, dq=None, dk=None, dv=None, scale=0.09, ws=FAKE, ws_bytes=None):
     if ws_bytes is None:
-        ws_bytes = lib.fa_fwd_fp8_workspace_size(B, H, N, 128)
+        ws_bytes = lib.fa_fwd_fp8_workspace_size(B, H, N, 128)   # >= the D = 64 size
     return lib.fa_fwd_fp8(q, k, v, o, lse, B, H, N, D,
                           ctypes.byref(layout) if layout is not None else None,
                           ctypes.byref(opts) if opts is not None else None, dq, dk, dv,
@@ -219,12 +219,14 @@ def test_fp8_workspace_size(lib):
     # V^T: B*H*D*ld bytes, ld = N rounded up to 16, rounded up to 256
     assert lib.fa_fwd_fp8_workspace_size(1, 2, 300, 128) == 2 * 128 * 304
     assert lib.fa_fwd_fp8_workspace_size(3, 1, 1, 128) == 3 * 128 * 16
-    assert lib.fa_fwd_fp8_workspace_size(1, 1, 128, 64) == 0     # D must be 128
+    assert lib.fa_fwd_fp8_workspace_size(1, 1, 130, 64) == 64 * 144
+    assert lib.fa_fwd_fp8_workspace_size(1, 1, 128, 96) == 0     # D is 64 or 128
     assert lib.fa_fwd_fp8_workspace_size(0, 1, 128, 128) == 0
 
 
 @pytest.mark.parametrize("kw,status", [
-    ({"D": 64}, fattn.FA_ERR_UNSUPPORTED),
+    ({"D": 96}, fattn.FA_ERR_UNSUPPORTED),
+    ({"D": 32}, fattn.FA_ERR_UNSUPPORTED),
     ({"q": NULL}, fattn.FA_ERR_INVALID_ARG),
     ({"k": FAKE + 8}, fattn.FA_ERR_INVALID_ARG),
     ({"N": 0}, fattn.FA_ERR_INVALID_ARG),

@@ -19,6 +19,7 @@ D = 128
 
 def run_fp8(d, B, H, N, scale, causal, opts=None, descale=True):
     q8, k8, v8 = (d[n].cuda() for n in ("q8", "k8", "v8"))
+    D = q8.shape[-1]
     desc = [d["descale_" + n].cuda() if descale else None for n in "qkv"]
     o = torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
@@ -48,20 +49,53 @@ def check(d, o, lse, scale, causal, rows=None, descale=True, slopes=None, **kw):
     return ratio
 
 
-@pytest.mark.parametrize("B,H,N,causal,seed", [
-    (1, 2, 300, False, 21),
-    (1, 2, 300, True, 22),
-    (2, 3, 1000, True, 23),
-    (1, 1, 1, False, 24),
-    (1, 2, 129, True, 25),
-    (2, 1, 128 * 5 + 17, False, 26),
-    (1, 2, 2048, False, 27),
+@pytest.mark.parametrize("B,H,N,D,causal,seed", [
+    (1, 2, 300, 128, False, 21),
+    (1, 2, 300, 128, True, 22),
+    (2, 3, 1000, 128, True, 23),
+    (1, 1, 1, 128, False, 24),
+    (1, 2, 129, 128, True, 25),
+    (2, 1, 128 * 5 + 17, 128, False, 26),
+    (1, 2, 2048, 128, False, 27),
+    (1, 2, 300, 64, False, 41),
+    (2, 3, 1000, 64, True, 42),
+    (1, 1, 1, 64, True, 43),
+    (2, 1, 128 * 5 + 17, 64, False, 44),
+    (1, 2, 2048, 64, True, 45),
 ])
-def test_fp8_forward_within_the_e4m3_bound(B, H, N, causal, seed):
+def test_fp8_forward_within_the_e4m3_bound(B, H, N, D, causal, seed):
     d = W.make_fp8_inputs(W.custom(B, H, N, D, causal=causal, seed=seed, backward=False))
     scale = D ** -0.5
     o, lse = run_fp8(d, B, H, N, scale, causal)
     check(d, o, lse, scale, causal)
+
+
+def test_fp8_head_dim_64_window_alibi_and_block_mask():
+    B, H, N, D = 2, 2, 600, 64
+    d = W.make_fp8_inputs(W.custom(B, H, N, D, causal=True, seed=46, backward=False))
+    scale = D ** -0.5
+    slopes = torch.tensor([0.5, 0.03125], dtype=torch.float32)
+    opts = fattn.options((150, -1), slopes.cuda(), None)
+    o, lse = run_fp8(d, B, H, N, scale, True, opts)
+    check(d, o, lse, scale, True, slopes=slopes.numpy(), window=(150, -1))
+    T = (N + 127) // 128
+    mask = (np.random.default_rng(47).random((T, T)) < 0.6).astype(np.uint8)
+    opts = fattn.options((-1, -1), None, torch.from_numpy(mask).cuda())
+    o, lse = run_fp8(d, B, H, N, scale, False, opts)
+    check(d, o, lse, scale, False, block_mask=mask)
+
+
+def test_fp8_head_dim_64_api_layout_matches_contiguous_call_bit_for_bit():
+    B, H, N, D = 2, 3, 333, 64
+    d = W.make_fp8_inputs(W.custom(B, H, N, D, causal=False, seed=48, backward=False))
+    o_ref, lse_ref = run_fp8(d, B, H, N, 0.11, False)
+    q, k, v = (d[n + "8"].cuda().transpose(1, 2).contiguous() for n in "qkv")   # BNHD
+    o, lse = attention.flash_attn_fp8_func(q, k, v, softmax_scale=0.11,
+                                           descale_q=d["descale_q"].cuda(),
+                                           descale_k=d["descale_k"].cuda(),
+                                           descale_v=d["descale_v"].cuda(), return_lse=True)
+    assert torch.equal(o.transpose(1, 2), o_ref)
+    assert torch.equal(lse, lse_ref)
 
 
 def test_fp8_forward_is_deterministic():
