@@ -180,9 +180,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   const int n_q64 = (p.N + kQ64 - 1) / kQ64;
   // Head-major order, longest key tiles first within a head: the CTAs in
   // flight share one head's Q, dO and dQ accumulator in L2.
-  const int bh = static_cast<int>(blockIdx.x / n_kt);
+  // (tile-major instead when the streamed operands all fit in L2)
+  const int bh = static_cast<int>(p.tile_major ? blockIdx.x % p.BH : blockIdx.x / n_kt);
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
-  const int kt = static_cast<int>(blockIdx.x % n_kt);
+  const int kt = static_cast<int>(p.tile_major ? blockIdx.x / p.BH : blockIdx.x % n_kt);
   const int k0 = kt * kTile;
   const int wl = p.band.win_left, wr = p.band.win_right;
   int it_begin, it_last;  // 64-row query tiles whose band reaches this key tile
@@ -670,11 +671,12 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
   const int n_k64 = (p.N + kK64 - 1) / kK64;
   // Head-major; when keys are bounded on the right only (causal) later
   // query tiles see more keys and go first.
-  const int bh = static_cast<int>(blockIdx.x / n_qt);
+  // (tile-major instead when the streamed operands all fit in L2)
+  const int bh = static_cast<int>(p.tile_major ? blockIdx.x % p.BH : blockIdx.x / n_qt);
   const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
   const int wl = p.band.win_left, wr = p.band.win_right;
-  const int qt = (wl < 0 && wr >= 0) ? n_qt - 1 - static_cast<int>(blockIdx.x % n_qt)
-                                     : static_cast<int>(blockIdx.x % n_qt);
+  const int tile_idx = static_cast<int>(p.tile_major ? blockIdx.x / p.BH : blockIdx.x % n_qt);
+  const int qt = (wl < 0 && wr >= 0) ? n_qt - 1 - tile_idx : tile_idx;
   const int q0 = qt * kTile;
   int it_begin, it_last;  // 64-key tiles this query tile's band reaches
   band_key_tiles(q0, kTile, kK64, n_k64, wl, wr, it_begin, it_last);
@@ -936,14 +938,16 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
 // dQ convert
 // ---------------------------------------------------------------------------
 // acc is [BH][N][D] fp32; dq gets scale * acc in the caller's layout.  One
-// thread per 8 consecutive elements of a row.
-template <bool kBf16>
+// thread per 8 consecutive elements of a row.  The row -> (batch, head,
+// position) split uses 32-bit division whenever the row count allows: with
+// 64-bit division the index arithmetic, not HBM, set the kernel's pace.
+template <bool kBf16, int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
                                                          uint16_t* __restrict__ dq, RowStrides sdq,
-                                                         int N, int H, int D, long long n8,
-                                                         float scale) {
+                                                         int N, int H, long long n8, float scale) {
+  constexpr int g = D / 8;  // threads per row
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  const int g = D / 8;
+  const bool rows32 = n8 / g <= 0xffffffffLL;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
        t += stride) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
@@ -954,9 +958,18 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     o.z = pack2<kBf16>(b.x * scale, b.y * scale);
     o.w = pack2<kBf16>(b.z * scale, b.w * scale);
     const long long row = t / g;  // over BH * N
-    const long long bh = row / N, n = row % N;
-    *reinterpret_cast<uint4*>(dq + (bh / H) * sdq.batch + (bh % H) * sdq.head + n * sdq.seq +
-                              (t % g) * 8) = o;
+    long long n;
+    int bh;
+    if (rows32) {
+      const uint32_t r = static_cast<uint32_t>(row), q = r / static_cast<uint32_t>(N);
+      bh = static_cast<int>(q);
+      n = r - q * static_cast<uint32_t>(N);
+    } else {
+      bh = static_cast<int>(row / N);
+      n = row - static_cast<long long>(bh) * N;
+    }
+    const int bb = bh / H, hh = bh - bb * H;
+    *reinterpret_cast<uint4*>(dq + bb * sdq.batch + hh * sdq.head + n * sdq.seq + (t % g) * 8) = o;
   }
 }
 
@@ -984,7 +997,9 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kDqPipeThreads, smem, st>>>(a);
+  BwdLaunch b = a;  // streamed per head: K and V
+  b.tile_major = tile_major_order(a.band, 4LL * a.BH * a.N * a.D);
+  kern<<<static_cast<unsigned>(grid), kDqPipeThreads, smem, st>>>(b);
   return cudaGetLastError();
 }
 
@@ -997,7 +1012,9 @@ cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kPipeThreads, smem, st>>>(a);
+  BwdLaunch b = a;  // streamed per head: Q, dO and, atomic mode, the fp32 dQ accumulator
+  b.tile_major = tile_major_order(a.band, (kAtomic ? 8LL : 4LL) * a.BH * a.N * a.D);
+  kern<<<static_cast<unsigned>(grid), kPipeThreads, smem, st>>>(b);
   return cudaGetLastError();
 }
 
@@ -1066,10 +1083,13 @@ cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N,
   if (blocks < 1) blocks = 1;
   auto* d16 = static_cast<uint16_t*>(dq);
   const unsigned g = static_cast<unsigned>(blocks);
-  if (bf16)
-    dq_convert_kernel<true><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, D, n8, scale);
-  else
-    dq_convert_kernel<false><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, D, n8, scale);
+  if (D == 64) {
+    if (bf16) dq_convert_kernel<true, 64><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, n8, scale);
+    else dq_convert_kernel<false, 64><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, n8, scale);
+  } else {
+    if (bf16) dq_convert_kernel<true, 128><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, n8, scale);
+    else dq_convert_kernel<false, 128><<<g, 256, 0, st>>>(acc, d16, sdq, N, H, n8, scale);
+  }
   return cudaGetLastError();
 }
 

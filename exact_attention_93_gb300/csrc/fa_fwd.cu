@@ -39,7 +39,16 @@
 // K/V stream over the union of their key-tile ranges.  With an ALiBi slope
 // (flash_attn_func alibi_slopes) every score gets -slope * |i - j| added
 // before the softmax.  The grid runs head-major, the longest query-tile
-// pairs of a head first, so the CTAs in flight share one head's K and V in L2.
+// pairs of a head first, so the CTAs in flight share one head's K and V in L2
+// (tile-major for short causal sequences whose K and V all fit in L2).
+//
+// Work units: a CTA may process several query-tile pairs in turn.  With
+// short sequences the per-CTA costs (barrier set-up, TMEM allocation, the
+// first loads, the epilogue, the launch of the next CTA) weigh as much as
+// the key-tile loop, so the grid then holds one resident CTA per SM: the
+// next unit's Q and first K/V land and its first scores are computed while
+// the softmax warps still run the previous unit's epilogue.  All barrier
+// phases count across units.
 //
 // 8-bit operands (the FP8 forward FlashAttention-3 adds, which the "Flash
 // Attention" wiki page and the v3 row of "FlashAttention 深入" list): Q, K
@@ -70,12 +79,18 @@ struct FwdSmem {
   static constexpr int kTileBytes = kBlocks * kBlockBytes;  // also V^T: D rows x 128 B
   static constexpr int kOBlocks = D / 64;                   // 16-bit O: 64-column blocks
   static constexpr int kOBlockBytes = kTile * 128;          // 128 rows x 128 B
+  // O staging of its own (8-bit operands, or D = 64 where it fits beside the
+  // tiles); 16-bit D = 128 stages O in the tile's spent Q buffer
+  static constexpr bool kOwnStage = kFp8 || D == 64;
+  // Q buffer sets: with O staged apart, a resident CTA loads the next unit's
+  // Q into the other set while the current unit runs
+  static constexpr int kQSets = kOwnStage ? 2 : 1;
   // tiles A and B; with 16-bit operands each is reused as its O staging
-  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t q[kQSets][2][kTileBytes];  // [set][tile]
   alignas(1024) uint8_t k[2][kTileBytes];
   alignas(1024) uint8_t v[2][kTileBytes];  // 8-bit: V^T, D rows x 128 keys
-  alignas(1024) uint8_t o[kFp8 ? 2 : 1][kFp8 ? kOBlocks * kOBlockBytes : 16];
-  uint64_t q_full;
+  alignas(1024) uint8_t o[kOwnStage ? 2 : 1][kOwnStage ? kOBlocks * kOBlockBytes : 16];
+  uint64_t q_full[kQSets], q_empty[kQSets];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   uint64_t drain;
@@ -114,6 +129,13 @@ struct KeyWalk {
   }
 };
 
+// One work unit: query tiles 2 pt and 2 pt + 1 of (batch, head) bh.
+struct FwdUnit {
+  int bh, hh, bb, pt;  // hh, bb: TMA coordinates of (batch, head)
+  int lo[2], hi[2];    // key tiles [lo_t, hi_t] of query tile 2 pt + t (lo > hi: none)
+  int n_q_here;        // query tiles inside the sequence (1 or 2)
+};
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort_flag) {
   bool ok = mbar_wait(bar, parity, err, abort_flag);
@@ -140,10 +162,13 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
 }
 
 // kBf16: the 16-bit type of O (and of Q, K, V unless kFp8, where they are
-// e4m3 bytes and V arrives transposed).
-template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8>
+// e4m3 bytes and V arrives transposed).  kResident: the CTAs stay resident
+// and take several work units each; otherwise each CTA takes one.
+template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8, bool kResident>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdLaunch p) {
   using Smem = FwdSmem<D, kSparse, kFp8>;
+  static_assert(!kResident || (Smem::kOwnStage && !kSparse),
+                "resident CTAs: dense, O staged apart from Q");
   constexpr int kColsPerBlock = kFp8 ? 128 : 64;  // elements in a 128-byte block
   // 8-bit D = 64: Q and K rows are 64 bytes, in 64-byte-swizzled tiles
   constexpr bool kRows64 = Smem::kRowBytes < 128;
@@ -161,42 +186,70 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 
   const int n_q_tiles = (p.N + kTile - 1) / kTile;
   const int n_pairs = (n_q_tiles + 1) / 2;
-  const int bh = static_cast<int>(blockIdx.x / n_pairs);
-  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
+  const int n_kv = (p.N + kTile - 1) / kTile;
+  const long long n_units = static_cast<long long>(n_pairs) * p.BH;
   const int wl = p.band.win_left, wr = p.band.win_right;
   // With keys bounded on the right only (causal), later pairs see more keys:
   // they go first.
   const bool later_longer = wl < 0 && wr >= 0;
-  const int pt = later_longer ? n_pairs - 1 - static_cast<int>(blockIdx.x % n_pairs)
-                              : static_cast<int>(blockIdx.x % n_pairs);
-  const int n_kv = (p.N + kTile - 1) / kTile;
-  // Key tiles [lo_t, hi_t] each query tile multiplies (empty, lo > hi, when
-  // tile B lies past the end).  lo and hi never decrease from A to B, and
-  // each range holds the tile's diagonal, so their union is contiguous.
-  int lo[2], hi[2];
+  // With G CTAs, CTA c takes unit k G + c in even rounds k and k G + G-1-c in
+  // odd ones: one unit each when the grid covers them all; resident CTAs
+  // walk the longest-first order back and forth, so that long and short
+  // units even out over the rounds.
+  auto unit_of = [&](int k) -> long long {
+    const long long G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+  };
+  auto decode = [&](long long u, FwdUnit& w) {
+    w.bh = static_cast<int>(p.tile_major ? u % p.BH : u / n_pairs);
+    const int idx = static_cast<int>(p.tile_major ? u / p.BH : u % n_pairs);
+    w.hh = w.bh % p.H;
+    w.bb = w.bh / p.H;
+    w.pt = later_longer ? n_pairs - 1 - idx : idx;
+    // lo and hi never decrease from tile A to B, and each range holds the
+    // tile's diagonal, so their union is contiguous.
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt = 2 * pt + t;
-    if (qt >= n_q_tiles) {
-      lo[t] = 1;
-      hi[t] = 0;
-    } else {
-      band_key_tiles(qt * kTile, kTile, kTile, n_kv, wl, wr, lo[t], hi[t]);
+    for (int t = 0; t < 2; ++t) {
+      const int qt = 2 * w.pt + t;
+      if (qt >= n_q_tiles) {
+        w.lo[t] = 1;
+        w.hi[t] = 0;
+      } else {
+        band_key_tiles(qt * kTile, kTile, kTile, n_kv, wl, wr, w.lo[t], w.hi[t]);
+      }
     }
-  }
-  const int n_q_here = hi[1] >= lo[1] ? 2 : 1;
-  KeyWalk<kSparse> walk{lo[0], hi[0], lo[1], hi[1], max(hi[0], hi[1]), n_kv,
-                        TileSet{s.key_tiles[0], n_kv},
-                        TileSet{s.key_tiles[kSparse ? 1 : 0], n_kv},
-                        TileSet{s.key_tiles[kSparse ? 2 : 0], n_kv}};
+    w.n_q_here = w.hi[1] >= w.lo[1] ? 2 : 1;
+  };
+  auto walk_of = [&](const FwdUnit& w) {
+    return KeyWalk<kSparse>{w.lo[0], w.hi[0], w.lo[1], w.hi[1], max(w.hi[0], w.hi[1]), n_kv,
+                            TileSet{s.key_tiles[0], n_kv},
+                            TileSet{s.key_tiles[kSparse ? 1 : 0], n_kv},
+                            TileSet{s.key_tiles[kSparse ? 2 : 0], n_kv}};
+  };
+  // Calls fn(k, u) for this CTA's units in order while it returns true.  A
+  // CTA with one unit runs it as straight-line code: a loop around the
+  // softmax would hold more of its state in registers.
+  auto for_each_unit = [&](auto&& fn) {
+    if constexpr (kResident) {
+      for (int k = 0;; ++k) {
+        const long long u = unit_of(k);
+        if (u >= n_units || !fn(k, u)) break;
+      }
+    } else {
+      fn(0, static_cast<long long>(blockIdx.x));
+    }
+  };
   if constexpr (kSparse) {
-    // the block mask, intersected with each tile's band range
-    const int qa = 2 * pt, qb = 2 * pt + 1;
+    // One unit per CTA: the block mask, intersected with each tile's band
+    // range.
+    FwdUnit w;
+    decode(blockIdx.x, w);
+    const int qa = 2 * w.pt, qb = 2 * w.pt + 1;
     auto in_a = [&](int j) {
-      return j >= lo[0] && j <= hi[0] && block_kept(p.band, bh, p.H, n_kv, qa, j);
+      return j >= w.lo[0] && j <= w.hi[0] && block_kept(p.band, w.bh, p.H, n_kv, qa, j);
     };
     auto in_b = [&](int j) {
-      return j >= lo[1] && j <= hi[1] && block_kept(p.band, bh, p.H, n_kv, qb, j);
+      return j >= w.lo[1] && j <= w.hi[1] && block_kept(p.band, w.bh, p.H, n_kv, qb, j);
     };
     fill_tile_set(s.key_tiles[0], n_kv, in_a);
     fill_tile_set(s.key_tiles[1], n_kv, in_b);
@@ -204,7 +257,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   }
 
   if (tid == 0) {
-    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < Smem::kQSets; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
@@ -233,43 +289,71 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       tma_prefetch_desc(&p.map_q);
       tma_prefetch_desc(&p.map_k);
       tma_prefetch_desc(&p.map_v);
-      mbar_arrive_expect_tx(&s.q_full, n_q_here * Smem::kTileBytes);
-      for (int t = 0; t < n_q_here; ++t)
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.q[t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full,
-                      kb * kColsPerBlock, (2 * pt + t) * kTile, hh, bb);
-      int issued = 0;
-      for (int j = walk.first(), jj = 0; j < walk.n; j = walk.next(j), ++jj) {
-        const int st = jj & 1;  // jj: position in the stream
-        const uint32_t u = static_cast<uint32_t>(jj >> 1);
-        if (jj >= 2 && !mbar_wait(&s.k_empty[st], (u - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
-        for (int kb = 0; kb < Smem::kBlocks; ++kb)
-          tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st],
-                      kb * kColsPerBlock, j * kTile, hh, bb);
-        if (jj >= 2 && !mbar_wait(&s.v_empty[st], (u - 1) & 1, p.err, abort_flag)) {
-          issued = jj * 2 + 1;
-          break;
-        }
-        mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
-        if constexpr (kFp8) {
-          // V^T rows d = 0..D-1, keys j*128 .. j*128+127
-          tma_load_4d(s.v[st], &p.map_v, &s.v_full[st], j * kTile, 0, hh, bb);
-        } else {
+      uint32_t kv = 0;      // K/V tiles loaded so far, over all units (ring position)
+      int q_rounds = 0;     // Q loads issued
+      long long loads = 0;  // K and V loads issued (K of ring position n is load 2n)
+      for_each_unit([&](int k, long long u) -> bool {
+        FwdUnit w;
+        decode(u, w);
+        const KeyWalk<kSparse> walk = walk_of(w);
+        // The running counters are copied in and out, so that the key-tile
+        // loop works on registers.
+        uint32_t ring = kv;
+        long long n_loads = loads;
+        // Unit k's Q goes into set k % kQSets once the last S product of the
+        // unit that used the set before has read it.
+        const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;
+        if (q_use > 0 && !mbar_wait(&s.q_empty[qs], (q_use - 1) & 1, p.err, abort_flag))
+          return false;
+        mbar_arrive_expect_tx(&s.q_full[qs], w.n_q_here * Smem::kTileBytes);
+        for (int t = 0; t < w.n_q_here; ++t)
           for (int kb = 0; kb < Smem::kBlocks; ++kb)
-            tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
-                        j * kTile, hh, bb);
+            tma_load_4d(s.q[qs][t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full[qs],
+                        kb * kColsPerBlock, (2 * w.pt + t) * kTile, w.hh, w.bb);
+        q_rounds = k + 1;
+        bool stop = false;
+        for (int j = walk.first(); j < walk.n; j = walk.next(j), ++ring) {
+          const int st = ring & 1;
+          const uint32_t use = ring >> 1;  // earlier uses of this stage
+          if (ring >= 2 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, p.err, abort_flag)) {
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
+          for (int kb = 0; kb < Smem::kBlocks; ++kb)
+            tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st],
+                        kb * kColsPerBlock, j * kTile, w.hh, w.bb);
+          ++n_loads;
+          if (ring >= 2 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, p.err, abort_flag)) {
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
+          if constexpr (kFp8) {
+            // V^T rows d = 0..D-1, keys j*128 .. j*128+127
+            tma_load_4d(s.v[st], &p.map_v, &s.v_full[st], j * kTile, 0, w.hh, w.bb);
+          } else {
+            for (int kb = 0; kb < Smem::kBlocks; ++kb)
+              tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
+                          j * kTile, w.hh, w.bb);
+          }
+          ++n_loads;
         }
-        issued = jj * 2 + 2;
-      }
+        kv = ring;
+        loads = n_loads;
+        return !stop;
+      });
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's smem goes away.
         int zero = 0;
-        mbar_wait(&s.q_full, 0, p.err, &zero, 100000000ull);
-        for (int t = max(0, issued - 4); t < issued; ++t) {
-          const int j = t >> 1, st = j & 1;
-          mbar_wait((t & 1) ? &s.v_full[st] : &s.k_full[st], (j >> 1) & 1, p.err, &zero,
+        for (int r = max(0, q_rounds - Smem::kQSets); r < q_rounds; ++r)
+          mbar_wait(&s.q_full[r % Smem::kQSets], (r / Smem::kQSets) & 1, p.err, &zero,
                     100000000ull);
+        for (long long t = loads > 4 ? loads - 4 : 0; t < loads; ++t) {
+          const long long n = t >> 1;  // ring position
+          const int st = static_cast<int>(n & 1);
+          mbar_wait((t & 1) ? &s.v_full[st] : &s.k_full[st], static_cast<uint32_t>((n >> 1) & 1),
+                    p.err, &zero, 100000000ull);
         }
       }
     }
@@ -281,8 +365,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
       constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, D) : idesc_f16(128, D, ab, 0, 1);
       // Operand descriptors are built once and advanced by constant offsets.
-      const uint64_t dq0 = kRows64 ? smem_desc_sw64(smem_u32(s.q[0]), 16, 512)
-                                   : smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
+      const uint64_t dq0 = kRows64 ? smem_desc_sw64(smem_u32(s.q[0][0]), 16, 512)
+                                   : smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
       const uint64_t dk0 = kRows64 ? smem_desc_sw64(smem_u32(s.k[0]), 16, 512)
                                    : smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t dv0 =
@@ -290,125 +374,160 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       // One product step covers 32 bytes of each row: 16 elements of 16 bits,
       // 32 of 8 bits.
       constexpr int kStepElems = kFp8 ? 32 : 16;
-      // S_t = Q_t K^T into tile t's S columns, K from stage kst
-      auto issue_s = [&](int t, int kst) {
-        const uint64_t dq = desc_add(dq0, t * Smem::kTileBytes);
-        const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
-          const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-          mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
-                       kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s.s_full[t]);
-      };
       // P step kk of V tile stage st: 16-bit V advances kStepElems rows of
       // 128 bytes, 8-bit V^T 32 bytes within each row.
       auto v_step = [](uint64_t dv, int kk) {
         return kFp8 ? desc_add(dv, kk * 32) : desc_add(dv, kk * kStepElems * 128);
       };
-      const int jf = walk.first();
-      // with nothing to multiply (an empty block-sparse pair) no K arrives
-      bool ok = mbar_wait(&s.q_full, 0, p.err, abort_flag) &&
-                (jf >= walk.n || mbar_wait(&s.k_full[0], 0, p.err, abort_flag));
-      if (ok && jf < walk.n) {
+      uint32_t kv_run = 0;              // K/V tiles of earlier units (ring position)
+      int base0_run = 0, base1_run = 0;  // P V products of tiles A, B in earlier units
+      for_each_unit([&](int k, long long u) -> bool {
+        FwdUnit w;
+        decode(u, w);
+        const KeyWalk<kSparse> walk = walk_of(w);
+        const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;  // this unit's Q set
+        // register copies of the running counters for this unit's loops
+        const uint32_t kv = kv_run;
+        const int base0 = base0_run, base1 = base1_run;
+        // S products of this unit still to issue; with resident CTAs the
+        // last one's commit hands the Q buffers to the next unit's loads.
+        [[maybe_unused]] int s_left = walk.count_of(0) + walk.count_of(1);
+        // S_t = Q_t K^T into tile t's S columns, K from stage kst
+        auto issue_s = [&](int t, int kst) {
+          const uint64_t dq = desc_add(dq0, (qs * 2 + t) * Smem::kTileBytes);
+          const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
+            const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+            mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
+                         kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s.s_full[t]);
+          if constexpr (kResident)
+            if (--s_left == 0) tc_commit(&s.q_empty[qs]);
+        };
+        const int jf = walk.first();
+        // with nothing to multiply (an empty block-sparse pair) no K arrives
+        bool ok = mbar_wait(&s.q_full[qs], q_use & 1, p.err, abort_flag) &&
+                  (jf >= walk.n || mbar_wait(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
+        if (!ok) return false;
+        if (jf >= walk.n) {
+          if constexpr (kResident) tc_commit(&s.q_empty[qs]);
+          return true;
+        }
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (walk.has(t, jf)) issue_s(t, 0);
-        tc_commit(&s.k_empty[0]);
-      }
-      if constexpr (!kSparse) {
-        // dense: each tile's key tiles are the range [lo_t, hi_t]
-        const int j_first = jf, j_last = walk.last;
-        for (int j = j_first; ok && j <= j_last; ++j) {
-          const int jj = j - j_first;
-          const int st = jj & 1;
-          if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
-          bool k_next = false;  // K_{j+1} has landed
-          for (int t = 0; ok && t < 2; ++t) {
-            const int lt = t ? lo[1] : lo[0], ht = t ? hi[1] : hi[0];
-            const bool active = j >= lt && j <= ht;
-            // S_t(j+1) is next: after PV_t(j), or as the first product of a
-            // tile whose range starts at j + 1
-            const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
-            if (active) {
-              if (!mbar_wait(&s.p_full[t], (j - lt) & 1, p.err, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // O_t += P_t(j) V_j, with P read from tile t's S columns
-              const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-#pragma unroll
-              for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
-                             idPV, (j > lt || kk > 0) ? 1u : 0u);
-              tc_commit(&s.o_done[t]);
+          if (walk.has(t, jf)) issue_s(t, kv & 1);
+        tc_commit(&s.k_empty[kv & 1]);
+        int n_stream = 0;  // key tiles in this unit's K/V stream
+        if constexpr (!kSparse) {
+          // dense: each tile's key tiles are the range [lo_t, hi_t]
+          const int j_first = jf, j_last = walk.last;
+          for (int j = j_first; ok && j <= j_last; ++j) {
+            const uint32_t g = kv + static_cast<uint32_t>(j - j_first);  // ring position of j
+            const int st = g & 1;
+            if (!mbar_wait(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
             }
-            if (s_next) {
-              if (!k_next) {
-                if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err,
+            bool k_next = false;  // K_{j+1} has landed
+            for (int t = 0; ok && t < 2; ++t) {
+              // (selects, not indexing: a dynamic index would put w in local memory)
+              const int lt = t ? w.lo[1] : w.lo[0], ht = t ? w.hi[1] : w.hi[0];
+              const bool active = j >= lt && j <= ht;
+              // S_t(j+1) is next: after PV_t(j), or as the first product of
+              // a tile whose range starts at j + 1
+              const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
+              if (active) {
+                if (!mbar_wait(&s.p_full[t], ((t ? base1 : base0) + j - lt) & 1, p.err,
                                abort_flag)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                k_next = true;
-              }
-              issue_s(t, (jj + 1) & 1);  // after the PV product that read P_t(j)
-            }
-          }
-          tc_commit(&s.v_empty[st]);
-          if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
-        }
-      } else {
-        // block-sparse: each tile's key tiles are a set; counters give the
-        // p_full phases
-        int c0 = 0, c1 = 0;  // P V products issued for tile A, B (p_full phases)
-        for (int j = jf, jj = 0, jn = 0; ok && j < walk.n; j = jn, ++jj) {
-          jn = walk.next(j);  // the stream's next key tile
-          const int st = jj & 1;
-          if (!mbar_wait(&s.v_full[st], (jj >> 1) & 1, p.err, abort_flag)) break;
-          bool k_next = false;  // K of tile jn has landed
-          for (int t = 0; ok && t < 2; ++t) {
-            const bool active = walk.has(t, j);
-            // S_t of tile jn follows PV_t(j), or starts a tile that joins at jn
-            const bool s_next = jn < walk.n && walk.has(t, jn);
-            if (active) {
-              const int ct = t ? c1 : c0;
-              if (!mbar_wait(&s.p_full[t], ct & 1, p.err, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // O_t += P_t(j) V_j, with P read from tile t's S columns
-              const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+                // O_t += P_t(j) V_j, with P read from tile t's S columns
+                const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
-              for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
-                             idPV, (ct > 0 || kk > 0) ? 1u : 0u);
-              tc_commit(&s.o_done[t]);
-              if (t)
-                ++c1;
-              else
-                ++c0;
+                for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                  mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                               idPV, (j > lt || kk > 0) ? 1u : 0u);
+                tc_commit(&s.o_done[t]);
+              }
+              if (s_next) {
+                if (!k_next) {
+                  if (!mbar_wait(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                                 abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  k_next = true;
+                }
+                issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
+              }
             }
-            if (s_next) {
-              if (!k_next) {
-                if (!mbar_wait(&s.k_full[(jj + 1) & 1], ((jj + 1) >> 1) & 1, p.err, abort_flag)) {
+            tc_commit(&s.v_empty[st]);
+            if (k_next) tc_commit(&s.k_empty[(g + 1) & 1]);
+          }
+          n_stream = j_last - j_first + 1;
+        } else {
+          // block-sparse: each tile's key tiles are a set; counters give the
+          // p_full phases
+          int c0 = 0, c1 = 0;  // P V products issued for tile A, B
+          for (int j = jf, jn = 0; ok && j < walk.n; j = jn, ++n_stream) {
+            jn = walk.next(j);  // the stream's next key tile
+            const uint32_t g = kv + static_cast<uint32_t>(n_stream);
+            const int st = g & 1;
+            if (!mbar_wait(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
+            bool k_next = false;  // K of tile jn has landed
+            for (int t = 0; ok && t < 2; ++t) {
+              const bool active = walk.has(t, j);
+              // S_t of tile jn follows PV_t(j), or starts a tile that joins at jn
+              const bool s_next = jn < walk.n && walk.has(t, jn);
+              if (active) {
+                const int ct = t ? c1 : c0;
+                if (!mbar_wait(&s.p_full[t], ((t ? base1 : base0) + ct) & 1, p.err, abort_flag)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                k_next = true;
+                // O_t += P_t(j) V_j, with P read from tile t's S columns
+                const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                  mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                               idPV, (ct > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&s.o_done[t]);
+                if (t)
+                  ++c1;
+                else
+                  ++c0;
               }
-              issue_s(t, (jj + 1) & 1);  // after the PV product that read P_t(j)
+              if (s_next) {
+                if (!k_next) {
+                  if (!mbar_wait(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                                 abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  k_next = true;
+                }
+                issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
+              }
             }
+            tc_commit(&s.v_empty[st]);
+            if (k_next) tc_commit(&s.k_empty[(g + 1) & 1]);
           }
-          tc_commit(&s.v_empty[st]);
-          if (k_next) tc_commit(&s.k_empty[(jj + 1) & 1]);
         }
-      }
+        kv_run = kv + static_cast<uint32_t>(n_stream);
+        base0_run = base0 + walk.count_of(0);
+        base1_run = base1 + walk.count_of(1);
+        return ok;
+      });
       // Every MMA issued above completes before TMEM is released.
       tc_commit(&s.drain);
       int zero = 0;
@@ -418,210 +537,224 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;          // query tile of this group (0 = A, 1 = B)
     const int r = tid & 127;          // row within the tile and TMEM lane
-    const int q0 = (2 * pt + t) * kTile;
-    const int i = q0 + r;
-    const int n_tiles = walk.count_of(t);
-    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + t * 128, tO = tbase + 256 + t * D;
-    // 8-bit operands carry per-(batch, head) dequantisation factors: Q and K
-    // scale the scores, V scales O.
-    float sl2 = p.scale_log2, v_descale = 1.f;
-    if constexpr (kFp8) {
-      if (p.descale_q) sl2 *= p.descale_q[bh];
-      if (p.descale_k) sl2 *= p.descale_k[bh];
-      if (p.descale_v) v_descale = p.descale_v[bh];
-    }
-    const bool pos_scale = sl2 > 0.f;
-    float m = -INFINITY;  // reference maximum, log2 units
-    float l = 0.f;        // running sum of 2^(t - m)
-    bool ok = true;
-    for (int jj = 0, j = walk.first_of(t); jj < n_tiles; ++jj, j = walk.next_of(t, j)) {
-      if (!warp_wait(&s.s_full[t], jj & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
+    int base_run = 0;  // key tiles of this query tile in earlier units (barrier phases)
+    for_each_unit([&](int k, long long u) -> bool {
+      const int base = base_run;
+      FwdUnit w;
+      decode(u, w);
+      const KeyWalk<kSparse> walk = walk_of(w);
+      const int bh = w.bh, hh = w.hh, bb = w.bb;
+      const int q0 = (2 * w.pt + t) * kTile;
+      const int i = q0 + r;
+      const int n_tiles = walk.count_of(t);
+      const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
+      // 8-bit operands carry per-(batch, head) dequantisation factors: Q and K
+      // scale the scores, V scales O.
+      float sl2 = p.scale_log2, v_descale = 1.f;
+      if constexpr (kFp8) {
+        if (p.descale_q) sl2 *= p.descale_q[bh];
+        if (p.descale_k) sl2 *= p.descale_k[bh];
+        if (p.descale_v) v_descale = p.descale_v[bh];
       }
-      tc_fence_after();
-      float sv[kTile];
-      {
-        // All four loads in flight before the single wait.
-        uint32_t raw[kTile / 32][32];
-#pragma unroll
-        for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tS + lane_off + c * 32, raw[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < kTile / 32; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(raw[c][e]);
-      }
-      // Scores -> log2 units.  With a positive scale and no bias this is
-      // folded into the exponent below (one packed FMA per two scores);
-      // otherwise scale (and add the ALiBi bias) first.
-      const int k0 = j * kTile;
-      const bool prescale = kAlibi || !pos_scale;
-      if (kAlibi) {
-        const float d0 = static_cast<float>(k0 - i);  // key - query at column 0 (exact)
-        const bool below = k0 + kTile - 1 <= q0, above = k0 >= q0 + kTile - 1;
-        if (below || above) {
-          // The whole tile lies on one side of the diagonal: |key - i| is
-          // linear in the column, so the bias is B + D c, two columns per
-          // packed FMA.
-          const float sd = above ? nslope2 : -nslope2;
-          const uint64_t b2 = f32x2(sd * d0, sd * d0), dd2 = f32x2(sd, sd), s2 = f32x2(sl2, sl2);
-#pragma unroll
-          for (int c = 0; c < kTile; c += 2) {
-            const uint64_t bias = fma_f32x2(f32x2(static_cast<float>(c), static_cast<float>(c + 1)),
-                                            dd2, b2);
-            const float2 x = split_f32x2(fma_f32x2(f32x2(sv[c], sv[c + 1]), s2, bias));
-            sv[c] = x.x;
-            sv[c + 1] = x.y;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            sv[c] = fmaf(sv[c], sl2, nslope2 * fabsf(d0 + static_cast<float>(c)));
-        }
-      } else if (!pos_scale) {
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) sv[c] *= sl2;
-      }
-      if (band_cuts(q0, kTile, k0, kTile, p.band.win_left, p.band.win_right) ||
-          k0 + kTile > p.N) {
-        // this row's visible keys are first .. last
-        const int wl_ = p.band.win_left, wr_ = p.band.win_right;
-        const int first = wl_ < 0 ? 0 : i - wl_;
-        const int last = min(p.N - 1, wr_ < 0 ? p.N - 1 : i + wr_);
-        const int cf = first - k0, cl = last - k0;  // visible columns cf .. cl
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c < cf || c > cl) sv[c] = -INFINITY;
-      }
-      // Row maximum: eight independent chains of three-input max.
-      float mxs[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mxs[e] = sv[e];
-#pragma unroll
-      for (int c = 8; c < kTile; c += 16)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          mxs[e] = c + 8 < kTile ? fmax3(mxs[e], sv[c + e], sv[c + 8 + e]) : fmaxf(mxs[e], sv[c + e]);
-      const float mx = fmax3(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], mxs[5]),
-                             fmaxf(mxs[6], mxs[7]));
-      const float m_tile = prescale ? mx : mx * sl2;
-      const float m_new = fmaxf(m, m_tile);
-      const bool need = m_new > m + kThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
-        l *= alpha;
-        m = m_new;
-      }
-      if (jj > 0 && __any_sync(0xffffffffu, need)) {
-        // O currently holds sum_{j' < j} P V; it must be final before scaling.
-        if (!warp_wait(&s.o_done[t], (jj - 1) & 1, p.err, abort_flag)) {
+      const bool pos_scale = sl2 > 0.f;
+      float m = -INFINITY;  // reference maximum, log2 units
+      float l = 0.f;        // running sum of 2^(t - m)
+      bool ok = true;
+      for (int jj = 0, j = walk.first_of(t); jj < n_tiles; ++jj, j = walk.next_of(t, j)) {
+        if (!warp_wait(&s.s_full[t], (base + jj) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + lane_off + c * 32, o);
+        float sv[kTile];
+        {
+          // All four loads in flight before the single wait.
+          uint32_t raw[kTile / 32][32];
+#pragma unroll
+          for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tS + lane_off + c * 32, raw[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + lane_off + c * 32, o);
+          for (int c = 0; c < kTile / 32; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(raw[c][e]);
         }
-      }
-      const float mneg = (m == -INFINITY) ? 0.f : kPOffset - m;
-      // P = 2^(x * mult - m), two columns per packed FMA / add; the softmax
-      // warps share issue slots with the MMA warp, so fewer instructions
-      // here keep the tensor core fed.
-      const float mult = prescale ? 1.f : sl2;
-      const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
-      uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
-      uint32_t pk8[kFp8 ? 32 : 1];  // 8-bit P: four keys per column
+        // Scores -> log2 units.  With a positive scale and no bias this is
+        // folded into the exponent below (one packed FMA per two scores);
+        // otherwise scale (and add the ALiBi bias) first.
+        const int k0 = j * kTile;
+        const bool prescale = kAlibi || !pos_scale;
+        if (kAlibi) {
+          const float d0 = static_cast<float>(k0 - i);  // key - query at column 0 (exact)
+          const bool below = k0 + kTile - 1 <= q0, above = k0 >= q0 + kTile - 1;
+          if (below || above) {
+            // The whole tile lies on one side of the diagonal: |key - i| is
+            // linear in the column, so the bias is B + D c, two columns per
+            // packed FMA.
+            const float sd = above ? nslope2 : -nslope2;
+            const uint64_t b2 = f32x2(sd * d0, sd * d0), dd2 = f32x2(sd, sd), s2 = f32x2(sl2, sl2);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 z = split_f32x2(
-              fma_f32x2(f32x2(sv[h * 64 + 2 * c], sv[h * 64 + 2 * c + 1]), mult2, mneg2));
-          const float p0 = ex2_approx(z.x), p1 = ex2_approx(z.y);
-          sums[c & 1] = add_f32x2(sums[c & 1], f32x2(p0, p1));
-          if constexpr (kFp8) {
-            const uint32_t b2 = pack2_e4m3(p0, p1);
-            if (c & 1)
-              pk8[h * 16 + (c >> 1)] |= b2 << 16;
-            else
-              pk8[h * 16 + (c >> 1)] = b2;
+            for (int c = 0; c < kTile; c += 2) {
+              const uint64_t bias = fma_f32x2(f32x2(static_cast<float>(c), static_cast<float>(c + 1)),
+                                              dd2, b2);
+              const float2 x = split_f32x2(fma_f32x2(f32x2(sv[c], sv[c + 1]), s2, bias));
+              sv[c] = x.x;
+              sv[c + 1] = x.y;
+            }
           } else {
-            pk[c] = pack2<kBf16>(p0, p1);
+#pragma unroll
+            for (int c = 0; c < kTile; ++c)
+              sv[c] = fmaf(sv[c], sl2, nslope2 * fabsf(d0 + static_cast<float>(c)));
           }
+        } else if (!pos_scale) {
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) sv[c] *= sl2;
         }
-        if constexpr (!kFp8) tmem_st32(tS + lane_off + h * 32, pk);
-      }
-      if constexpr (kFp8) tmem_st32(tS + lane_off, pk8);
-      const float2 s0 = split_f32x2(sums[0]), s1 = split_f32x2(sums[1]);
-      l += (s0.x + s0.y) + (s1.x + s1.y);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&s.p_full[t]);
-    }
-
-    // ---------------------------------------------------------- epilogue
-    // Every thread of the group takes the same branch (a timeout in one warp
-    // must not leave the others waiting at the barrier below).
-    if (q0 < p.N) {
-      // A tile the block mask empties has O = 0 and LSE = -inf; its smem
-      // stage may be written once its Q load has landed.
-      const bool have = n_tiles > 0;
-      const bool mine =
-          ok && (have ? warp_wait(&s.o_done[t], (n_tiles - 1) & 1, p.err, abort_flag)
-                      : warp_wait(&s.q_full, 0, p.err, abort_flag));
-      if (named_bar_and(1 + t, 128, mine)) {
-        tc_fence_after();
-        const float inv_l = l > 0.f ? v_descale / l : 0.f;
-        // 16-bit operands: this tile's Q is no longer read
-        uint8_t* stage = kFp8 ? s.o[t] : s.q[t];
+        if (band_cuts(q0, kTile, k0, kTile, p.band.win_left, p.band.win_right) ||
+            k0 + kTile > p.N) {
+          // this row's visible keys are first .. last
+          const int wl_ = p.band.win_left, wr_ = p.band.win_right;
+          const int first = wl_ < 0 ? 0 : i - wl_;
+          const int last = min(p.N - 1, wr_ < 0 ? p.N - 1 : i + wr_);
+          const int cf = first - k0, cl = last - k0;  // visible columns cf .. cl
+#pragma unroll
+          for (int c = 0; c < kTile; ++c)
+            if (c < cf || c > cl) sv[c] = -INFINITY;
+        }
+        // Row maximum: eight independent chains of three-input max.
+        float mxs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mxs[e] = sv[e];
+#pragma unroll
+        for (int c = 8; c < kTile; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mxs[e] = c + 8 < kTile ? fmax3(mxs[e], sv[c + e], sv[c + 8 + e]) : fmaxf(mxs[e], sv[c + e]);
+        const float mx = fmax3(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], mxs[5]),
+                               fmaxf(mxs[6], mxs[7]));
+        const float m_tile = prescale ? mx : mx * sl2;
+        const float m_new = fmaxf(m, m_tile);
+        const bool need = m_new > m + kThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+          l *= alpha;
+          m = m_new;
+        }
+        if (jj > 0 && __any_sync(0xffffffffu, need)) {
+          // O currently holds sum_{j' < j} P V; it must be final before scaling.
+          if (!warp_wait(&s.o_done[t], (base + jj - 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (have) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
             tmem_ld32(tO + lane_off + c * 32, o);
             tmem_ld_wait();
-          } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack2<kBf16>(__uint_as_float(o[2 * e]) * inv_l,
-                                 __uint_as_float(o[2 * e + 1]) * inv_l);
-          // 32 columns = four 16-byte chunks of this row, 128-byte swizzle
-          uint8_t* blk = stage + (c >> 1) * Smem::kOBlockBytes + r * 128;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int cc = (c & 1) * 4 + ch;
-            *reinterpret_cast<uint4*>(blk + ((cc ^ (r & 7)) * 16)) =
-                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, o);
           }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (r == 0) {
-          for (int kb = 0; kb < Smem::kOBlocks; ++kb)
-            tma_store_4d(&p.map_o, stage + kb * Smem::kOBlockBytes, kb * 64, q0, hh, bb);
-          tma_store_commit();
-          tma_store_wait_all();
+        const float mneg = (m == -INFINITY) ? 0.f : kPOffset - m;
+        // P = 2^(x * mult - m), two columns per packed FMA / add; the softmax
+        // warps share issue slots with the MMA warp, so fewer instructions
+        // here keep the tensor core fed.
+        const float mult = prescale ? 1.f : sl2;
+        const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
+        uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
+        uint32_t pk8[kFp8 ? 32 : 1];  // 8-bit P: four keys per column
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 z = split_f32x2(
+                fma_f32x2(f32x2(sv[h * 64 + 2 * c], sv[h * 64 + 2 * c + 1]), mult2, mneg2));
+            const float p0 = ex2_approx(z.x), p1 = ex2_approx(z.y);
+            sums[c & 1] = add_f32x2(sums[c & 1], f32x2(p0, p1));
+            if constexpr (kFp8) {
+              const uint32_t b2 = pack2_e4m3(p0, p1);
+              if (c & 1)
+                pk8[h * 16 + (c >> 1)] |= b2 << 16;
+              else
+                pk8[h * 16 + (c >> 1)] = b2;
+            } else {
+              pk[c] = pack2<kBf16>(p0, p1);
+            }
+          }
+          if constexpr (!kFp8) tmem_st32(tS + lane_off + h * 32, pk);
         }
-        if (i < p.N)
-          p.lse[static_cast<long long>(bh) * p.N + i] =
-              have ? (m - kPOffset + lg2_approx(l)) * kLn2 : -INFINITY;
+        if constexpr (kFp8) tmem_st32(tS + lane_off, pk8);
+        const float2 s0 = split_f32x2(sums[0]), s1 = split_f32x2(sums[1]);
+        l += (s0.x + s0.y) + (s1.x + s1.y);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[t]);
       }
-    }
+
+      // ---------------------------------------------------------- epilogue
+      // Every thread of the group takes the same branch (a timeout in one warp
+      // must not leave the others waiting at the barrier below), and the same
+      // decision to go on to the next unit.
+      bool group_ok = ok;
+      if (q0 < p.N) {
+        // A tile the block mask empties has O = 0 and LSE = -inf; its smem
+        // stage may be written once its Q load has landed.
+        const bool have = n_tiles > 0;
+        const bool mine =
+            ok && (have ? warp_wait(&s.o_done[t], (base + n_tiles - 1) & 1, p.err, abort_flag)
+                        : warp_wait(&s.q_full[k % Smem::kQSets], (k / Smem::kQSets) & 1, p.err,
+                                    abort_flag));
+        group_ok = named_bar_and(1 + t, 128, mine);
+        if (group_ok) {
+          tc_fence_after();
+          const float inv_l = l > 0.f ? v_descale / l : 0.f;
+          // 16-bit D = 128: this tile's Q is no longer read
+          uint8_t* stage = Smem::kOwnStage ? s.o[t] : s.q[0][t];
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (have) {
+              tmem_ld32(tO + lane_off + c * 32, o);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack2<kBf16>(__uint_as_float(o[2 * e]) * inv_l,
+                                   __uint_as_float(o[2 * e + 1]) * inv_l);
+            // 32 columns = four 16-byte chunks of this row, 128-byte swizzle
+            uint8_t* blk = stage + (c >> 1) * Smem::kOBlockBytes + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              const int cc = (c & 1) * 4 + ch;
+              *reinterpret_cast<uint4*>(blk + ((cc ^ (r & 7)) * 16)) =
+                  make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + t, 128);
+          if (r == 0) {
+            for (int kb = 0; kb < Smem::kOBlocks; ++kb)
+              tma_store_4d(&p.map_o, stage + kb * Smem::kOBlockBytes, kb * 64, q0, hh, bb);
+            tma_store_commit();
+            tma_store_wait_all();
+          }
+          if (i < p.N)
+            p.lse[static_cast<long long>(bh) * p.N + i] =
+                have ? (m - kPOffset + lg2_approx(l)) * kLn2 : -INFINITY;
+        }
+      }
+      base_run = base + n_tiles;
+      return group_ok;
+    });
   }
 
   tc_fence_before();
@@ -632,18 +765,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   }
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8 = false>
-cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse, kFp8>;
+template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8, bool kResident>
+cudaError_t launch_fwd_grid(const FwdLaunch& b, long long grid, cudaStream_t stream) {
+  auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse, kFp8, kResident>;
   const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse, kFp8>)) + 1024;
   static std::atomic<uint64_t> configured{0};
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  const long long n_q_tiles = (a.N + kTile - 1) / kTile;
-  const long long grid = (n_q_tiles + 1) / 2 * a.BH;
-  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(a);
+  kern<<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(b);
   return cudaGetLastError();
+}
+
+template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8 = false>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  const long long n_q_tiles = (a.N + kTile - 1) / kTile;
+  const long long units = (n_q_tiles + 1) / 2 * a.BH;
+  if (units > INT_MAX) return cudaErrorInvalidConfiguration;
+  FwdLaunch b = a;  // streamed per head: K and V
+  b.tile_major = tile_major_order(a.band, 2LL * a.BH * a.N * a.D * (kFp8 ? 1 : 2));
+  // Resident CTAs, one per SM, for short sequences (at most 32 key tiles)
+  // with more units than SMs; the next unit's loads need the O staging of
+  // their own.
+  if constexpr (FwdSmem<D, kSparse, kFp8>::kOwnStage && !kSparse) {
+    if (n_q_tiles <= 32) {
+      int sms = 0;
+      const cudaError_t e = sm_count(&sms);
+      if (e != cudaSuccess) return e;
+      if (units > sms) return launch_fwd_grid<D, kBf16, kAlibi, kSparse, kFp8, true>(b, sms, stream);
+    }
+  }
+  return launch_fwd_grid<D, kBf16, kAlibi, kSparse, kFp8, false>(b, units, stream);
 }
 
 // V^T for the 8-bit forward: the P V product wants its B operand K-major

@@ -27,6 +27,19 @@ cudaError_t ensure_dynamic_smem(K kern, int bytes, std::atomic<uint64_t>& done) 
   return e;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+inline cudaError_t sm_count(int* out) {
+  static std::atomic<int> cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && (*out = cached[dev].load(std::memory_order_relaxed)) > 0)
+    return cudaSuccess;
+  e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cached[dev].store(*out, std::memory_order_relaxed);
+  return e;
+}
+
 constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 
 // Tensor maps are 4-D {D, N, H, B} over the caller's strides (D contiguous);
@@ -67,6 +80,7 @@ struct FwdLaunch {
   const float* descale_q;
   const float* descale_k;
   const float* descale_v;
+  int tile_major;  // grid order (tile_major_order)
   uint32_t* err;
 };
 
@@ -85,8 +99,20 @@ struct BwdLaunch {
   float scale, scale_log2;
   Band band;
   int bf16;
+  int tile_major;  // grid order (tile_major_order)
   uint32_t* err;
 };
+
+// Grid order of the attention kernels.  Head-major (all tiles of one head,
+// then the next) keeps the operands that a head's CTAs share in L2 while
+// they run.  When the tiles' lengths differ (a causal band: keys bounded on
+// the right only) and the operands every CTA streams fit in L2 together
+// (`streamed_bytes`), tile-major order (tile 0 of every head, then tile 1,
+// ...) is taken instead: with the longest tiles first, the short tiles fill
+// the tail rather than leave one head's longest tile to start last.
+inline int tile_major_order(const Band& band, long long streamed_bytes) {
+  return band.win_left < 0 && band.win_right >= 0 && streamed_bytes <= (64ll << 20);
+}
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t s);
 // Element strides of one [B, H, N, D] operand (D contiguous).
