@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 
 
 def test_more_than_65535_ctas_forward_and_backward():
-    # B * H = 66000 slices of N = 3: 66000 CTAs in every tile kernel
+    # B * H = 66000 slices of N = 3: 66000 CTAs in every backward tile kernel; the
+    # forward's 66000 work units run on resident CTAs, about 434 each
     w = W.custom(2, 33000, 3, 64, "bf16", causal=True, seed=41)
     inputs = W.make_inputs(w)
     g = {k: v.cuda() for k, v in inputs.items()}
