@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
           // from quadrants 0 and 1) and add it into the accumulator with one
           // bulk tensor reduction instead of 64 atomics per thread; rows
           // past N fall outside the tensor map and are dropped.
+          const int sb = j & 1;
           if (quad < 2) {
-            const int sb = j & 1;
             if (j >= 2 && !warp_wait(&s.stage_free[sb], ((j >> 1) - 1) & 1, p.err, abort_flag))
               break;
             float* stage = s.dq_stage[sb];
@@ -426,20 +426,22 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.stage_full[sb]);
-            if (warp == 8) {
-              bool issued = true;  // one lane issues; the warp leaves the loop together
-              if (lane == 0) {
-                issued = mbar_wait(&s.stage_full[sb], (j >> 1) & 1, p.err, abort_flag);
-                if (issued) {
-                  tma_reduce_add_4d(&p.map_dqacc, stage, 0, q0, hh, bb);
-                  tma_store_commit();
-                  // the reduction of tile j - 1 has read its buffer: free it
-                  tma_store_wait_read_all_but_newest();
-                  if (j >= 1) mbar_arrive(&s.stage_free[(j - 1) & 1]);
-                }
+          } else if (quad == 2) {
+            // Warp 10 (its TMEM rows hold no dQ at D = 64) issues the
+            // reduction, so the staging warps go straight on to the next
+            // buffer.
+            bool issued = true;  // one lane issues; the warp leaves the loop together
+            if (lane == 0) {
+              issued = mbar_wait(&s.stage_full[sb], (j >> 1) & 1, p.err, abort_flag);
+              if (issued) {
+                tma_reduce_add_4d(&p.map_dqacc, s.dq_stage[sb], 0, q0, hh, bb);
+                tma_store_commit();
+                // the reduction of tile j - 1 has read its buffer: free it
+                tma_store_wait_read_all_but_newest();
+                if (j >= 1) mbar_arrive(&s.stage_free[(j - 1) & 1]);
               }
-              if (!__all_sync(0xffffffffu, issued)) break;
             }
+            if (!__all_sync(0xffffffffu, issued)) break;
           }
         } else {
           float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
     }
     // the last bulk reductions must have read shared memory before it goes
-    if (kAtomicDq && D == 64 && warp == 8 && lane == 0) tma_store_wait_all();
+    if (kAtomicDq && D == 64 && warp == 10 && lane == 0) tma_store_wait_all();
   } else {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, query-column half
