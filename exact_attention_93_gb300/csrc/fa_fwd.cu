@@ -1,7 +1,8 @@
 // fa_fwd.cu -- exact attention forward for sm_103a.
 //
-// One CTA computes two 128-row query tiles (A and B, adjacent in one
-// (batch, head)), walking the key/value tiles with an online softmax
+// A work unit is two 128-row query tiles (A and B, adjacent in one
+// (batch, head)); a CTA computes one unit, or several in turn (below),
+// walking the key/value tiles with an online softmax
 // ("FlashAttention from scratch" walkthrough, l189.com, sec. 2.2 and 2.4;
 // "FlashAttention 深入", online softmax).  Parallelism is over query tiles
 // as well as (batch, head), the sequence-dimension split of FlashAttention-2
@@ -15,8 +16,9 @@
 //              same TMEM columns, rescales O in TMEM when m grows, and runs
 //              the epilogue (O / l through a swizzled smem tile and a TMA
 //              store; LSE = ln 2 * (m + log2 l)).
-//   warp 8     TMA producer: both Q tiles once, K and V tiles into two smem
-//              stages.
+//   warp 8     TMA producer: a unit's two Q tiles once (into one of two
+//              buffer sets when the CTA runs several units), K and V tiles
+//              into two smem stages.
 //   warp 9     MMA issuer (one thread).  For key tile j it issues
 //                O_A += P_A(j) V_j, S_A(j+1) = Q_A K_{j+1}^T,
 //                O_B += P_B(j) V_j, S_B(j+1) = Q_B K_{j+1}^T,
