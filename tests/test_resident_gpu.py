@@ -18,9 +18,10 @@ pytestmark = pytest.mark.gpu
 
 
 def forward(q, k, v, scale, causal, opts=None):
+    # NaN-filled outputs: a unit no CTA ran would leave NaN behind
     B, H, N, D = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
     fattn.fa_fwd_ex(q, k, v, o, lse, None, opts, B, H, N, D, scale, causal)
     return o, lse
 
@@ -41,6 +42,7 @@ def test_resident_forward_matches_oracle_and_single_head_calls(B, H, N, dtype, c
     o, lse = forward(q, k, v, w.scale, causal, opts)
     torch.cuda.synchronize()
     assert fattn.fa_device_error() == fattn.FA_OK
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()  # every unit ran
     heads = [(0, 0), (B - 1, H // 2), (B - 1, H - 1)]
     for b, h in heads:
         # the same head alone: one unit per CTA
@@ -73,14 +75,15 @@ def test_resident_fp8_forward(B, H, N, D, causal, seed):
         qq, kk, vv = (x[sl_b, sl_h].contiguous() for x in (q8, k8, v8))
         dd = [x[sl_b, sl_h].contiguous() for x in desc]
         b, h = qq.shape[:2]
-        o = torch.empty(b, h, N, D, dtype=torch.bfloat16, device="cuda")
-        lse = torch.empty(b, h, N, dtype=torch.float32, device="cuda")
+        o = torch.full((b, h, N, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((b, h, N), float("nan"), dtype=torch.float32, device="cuda")
         fattn.fa_fwd_fp8(qq, kk, vv, o, lse, None, None, b, h, N, D, scale, causal, *dd)
         return o, lse
 
     o, lse = run(slice(None), slice(None))
     torch.cuda.synchronize()
     assert fattn.fa_device_error() == fattn.FA_OK
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()  # every unit ran
     qd, kd, vd = ofp8.dequantise(d["q8"], d["k8"], d["v8"], d["descale_q"], d["descale_k"],
                                  d["descale_v"])
     for b, h in ((0, 0), (B - 1, H - 1)):
