@@ -24,7 +24,6 @@ import csv
 import hashlib
 import io
 import json
-import math
 import os
 import re
 import statistics

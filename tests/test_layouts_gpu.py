@@ -6,7 +6,6 @@ must reproduce the contiguous call bit for bit: the forward, the
 deterministic backward, and dK/dV of the atomic backward (whose dQ sums
 fp32 atomics in a run-dependent order).  The autograd entry points are
 checked against the fp64 oracle like every other path."""
-import numpy as np
 import pytest
 import torch
 
