@@ -410,8 +410,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         };
         const int jf = walk.first();
         // with nothing to multiply (an empty block-sparse pair) no K arrives
-        bool ok = mbar_wait(&s.q_full[qs], q_use & 1, p.err, abort_flag) &&
-                  (jf >= walk.n || mbar_wait(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
+        bool ok = mbar_wait_poll(&s.q_full[qs], q_use & 1, p.err, abort_flag) &&
+                  (jf >= walk.n || mbar_wait_poll(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
         if (!ok) return false;
         if (jf >= walk.n) {
           if constexpr (kResident) tc_commit(&s.q_empty[qs]);
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
           for (int j = j_first; ok && j <= j_last; ++j) {
             const uint32_t g = kv + static_cast<uint32_t>(j - j_first);  // ring position of j
             const int st = g & 1;
-            if (!mbar_wait(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+            if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
               ok = false;
               break;
             }
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               // a tile whose range starts at j + 1
               const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
               if (active) {
-                if (!mbar_wait(&s.p_full[t], ((t ? base1 : base0) + j - lt) & 1, p.err,
+                if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + j - lt) & 1, p.err,
                                abort_flag)) {
                   ok = false;
                   break;
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               }
               if (s_next) {
                 if (!k_next) {
-                  if (!mbar_wait(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                  if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
                                  abort_flag)) {
                     ok = false;
                     break;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             jn = walk.next(j);  // the stream's next key tile
             const uint32_t g = kv + static_cast<uint32_t>(n_stream);
             const int st = g & 1;
-            if (!mbar_wait(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+            if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
               ok = false;
               break;
             }
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               const bool s_next = jn < walk.n && walk.has(t, jn);
               if (active) {
                 const int ct = t ? c1 : c0;
-                if (!mbar_wait(&s.p_full[t], ((t ? base1 : base0) + ct) & 1, p.err, abort_flag)) {
+                if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + ct) & 1, p.err, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
               }
               if (s_next) {
                 if (!k_next) {
-                  if (!mbar_wait(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                  if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
                                  abort_flag)) {
                     ok = false;
                     break;
@@ -562,7 +562,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
       }
       const bool pos_scale = sl2 > 0.f;
       float m = -INFINITY;  // reference maximum, log2 units
-      float l = 0.f;        // running sum of 2^(t - m)
+      float l = 0.f;        // running sum of 2^(t - m), the LSE's
+      // The sum O is divided by, for 16-bit P.  O is made of P values
+      // rounded to 8 (bf16) or 11 (fp16) bits; dividing by their exact sum
+      // l would move O by the rounding of P times the V rows themselves,
+      // which is 2^-8 |V| where one key dominates a row: with a lagging
+      // reference maximum that key's P lies anywhere in [1, 256).  So lo
+      // takes the rounded value of each tile's largest P instead of its
+      // exact one, and, on tiles the mask cuts in a query tile whose rows
+      // see at most 128 keys (where every weight can be large), the rounded
+      // value of every P: the weights that dominate O then sum to one as
+      // rounded.  The LSE keeps the exact sum l.
+      float lo = 0.f;
+      const bool few_keys = [&] {
+        // the visible-key count of row i is concave in i: its minimum over
+        // the tile is at an end row (block masks that drop tiles: few)
+        if (kSparse && walk.count_of(t) < (t ? w.hi[1] - w.lo[1] : w.hi[0] - w.lo[0]) + 1)
+          return true;
+        auto count = [&](int row) {
+          const int first = wl < 0 ? 0 : max(0, row - wl);
+          const int last = min(p.N - 1, wr < 0 ? p.N - 1 : row + wr);
+          return last - first + 1;
+        };
+        return min(count(q0), count(min(q0 + kTile, p.N) - 1)) <= kTile;
+      }();
       bool ok = true;
       for (int jj = 0, j = walk.first_of(t); jj < n_tiles; ++jj, j = walk.next_of(t, j)) {
         if (!warp_wait(&s.s_full[t], (base + jj) & 1, p.err, abort_flag)) {
@@ -613,8 +636,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
           for (int c = 0; c < kTile; ++c) sv[c] *= sl2;
         }
-        if (band_cuts(q0, kTile, k0, kTile, p.band.win_left, p.band.win_right) ||
-            k0 + kTile > p.N) {
+        const bool masked =
+            band_cuts(q0, kTile, k0, kTile, p.band.win_left, p.band.win_right) || k0 + kTile > p.N;
+        if (masked) {
           // this row's visible keys are first .. last
           const int wl_ = p.band.win_left, wr_ = p.band.win_right;
           const int first = wl_ < 0 ? 0 : i - wl_;
@@ -642,6 +666,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         if (need) {
           alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
           l *= alpha;
+          lo *= alpha;
           m = m_new;
         }
         if (jj > 0 && __any_sync(0xffffffffu, need)) {
@@ -667,6 +692,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         // here keep the tensor core fed.
         const float mult = prescale ? 1.f : sl2;
         const uint64_t mult2 = f32x2(mult, mult), mneg2 = f32x2(mneg, mneg);
+        // the tile's largest P as the loop below computes it, and as rounded
+        float pmax_corr = 0.f;
+        if constexpr (!kFp8) {
+          const float pmax = ex2_approx(fmaf(mx, mult, mneg));
+          pmax_corr = unpack2<kBf16>(pack2<kBf16>(pmax, 0.f)).x - pmax;
+        }
         uint64_t sums[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};  // independent partial row sums
         uint32_t pk8[kFp8 ? 32 : 1];  // 8-bit P: four keys per column
 #pragma unroll
@@ -692,7 +723,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
         if constexpr (kFp8) tmem_st32(tS + lane_off, pk8);
         const float2 s0 = split_f32x2(sums[0]), s1 = split_f32x2(sums[1]);
-        l += (s0.x + s0.y) + (s1.x + s1.y);
+        const float tile_sum = (s0.x + s0.y) + (s1.x + s1.y);
+        l += tile_sum;
+        if constexpr (kFp8) {
+          lo += tile_sum;
+        } else if (masked && few_keys) {
+          // every P as rounded, read back from TMEM (rare tiles: the
+          // registers of the loop above are free by now)
+          tmem_st_wait();
+          uint64_t rs = f32x2(0.f, 0.f);
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pr[32];
+            tmem_ld32(tS + lane_off + h * 32, pr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float2 q2 = unpack2<kBf16>(pr[c]);
+              rs = add_f32x2(rs, f32x2(q2.x, q2.y));
+            }
+          }
+          const float2 r2 = split_f32x2(rs);
+          lo += r2.x + r2.y;
+        } else {
+          lo += tile_sum + pmax_corr;
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&s.p_full[t]);
@@ -714,7 +769,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         group_ok = named_bar_and(1 + t, 128, mine);
         if (group_ok) {
           tc_fence_after();
-          const float inv_l = l > 0.f ? v_descale / l : 0.f;
+          const float inv_l = lo > 0.f ? v_descale / lo : 0.f;
           // 16-bit D = 128: this tile's Q is no longer read
           uint8_t* stage = Smem::kOwnStage ? s.o[t] : s.q[0][t];
 #pragma unroll 1

@@ -70,6 +70,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// The same test without the suspend hint: a thread that is not ready
+// re-polls after the hardware's own short limit instead of sleeping until
+// the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Longest a single wait may take before the kernel gives up (ns).  Every
 // wait in a healthy launch ends in microseconds.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -85,6 +100,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) break;
+  }
+  atomicExch(err, kDevErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+// mbar_wait for a thread whose wake-up latency is on the critical path
+// (an MMA issuer whose products the other warps wait for): it polls rather
+// than sleeps, which wakes it a few hundred cycles sooner.  Same bound and
+// abort behaviour as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                               volatile int* abort_flag,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_poll(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_poll(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) break;
   }

@@ -1,0 +1,115 @@
+// unit_rates.cu -- per-SM throughput of the instructions the attention
+// kernels' elementwise steps are built from, measured in SM clock cycles.
+//
+// One 1024-thread block per SM (a large dynamic shared-memory request keeps
+// a second block off the SM); every thread runs kChains independent chains
+// of the instruction under test, so the unit, not latency, sets the pace.
+// Each block stamps clock64() around its loop; the rate of a block is
+// (operations it issued) / (cycles it took).  Prints one JSON line with the
+// median over blocks of each rate, in lanes (scalar results) per clock per
+// SM.
+#include <cstdio>
+#include <cstdint>
+#include <vector>
+#include <algorithm>
+#include <cuda_runtime.h>
+
+constexpr int kThreads = 1024, kChains = 8, kIters = 4096;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// kind 0: ex2.approx.ftz.f32 (one result per lane-instruction)
+// kind 1: cvt.rn.satfinite.e4m3x2.f32 (one instruction converts two values;
+//         counted per instruction)
+// kind 2: cvt.rn.bf16x2.f32 (counted per instruction)
+template <int kKind>
+__global__ void __launch_bounds__(kThreads, 1) rate_kernel(float seed, unsigned long long* cycles,
+                                                          uint32_t* sink) {
+  __shared__ float init;
+  __shared__ uint32_t results[kThreads];
+  if (threadIdx.x == 0) init = seed;
+  __syncthreads();
+  const unsigned long long t0 = clock64();
+  // The chains start from a value loaded after this barrier and end in a
+  // shared-memory store before the next one; neither can cross a barrier,
+  // so the whole loop runs between the two clock reads.
+  __syncthreads();
+  const float s0 = init;
+  float x[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) x[c] = s0 * (threadIdx.x + c + 1) * 1e-6f;
+  for (int it = 0; it < kIters; ++it) {
+#pragma unroll
+    for (int c = 0; c < kChains; ++c) {
+      if constexpr (kKind == 0) {
+        x[c] = ex2(x[c]);
+      } else {
+        const uint32_t r = kKind == 1 ? cvt_e4m3x2(x[c], -x[c]) : cvt_bf16x2(x[c], -x[c]);
+        // feed the result back so that each conversion waits for the last
+        x[c] = __uint_as_float((r & 0x007F00FFu) | 0x3F000000u);
+      }
+    }
+  }
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) acc ^= __float_as_uint(x[c]);
+  results[threadIdx.x] = acc;
+  __syncthreads();
+  const unsigned long long t1 = clock64();
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+  if (results[(threadIdx.x + 1) % kThreads] == 0x12345678u) sink[0] = acc;  // keeps them live
+}
+
+template <int kKind>
+static double measure(int sms) {
+  unsigned long long* cyc = nullptr;
+  uint32_t* sink = nullptr;
+  cudaMalloc(&cyc, sizeof(unsigned long long) * sms);
+  cudaMalloc(&sink, sizeof(uint32_t));
+  const int smem = 160 * 1024;  // one block per SM
+  if (cudaFuncSetAttribute(rate_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return -1.0;
+  rate_kernel<kKind><<<sms, kThreads, smem>>>(0.5f, cyc, sink);  // warm-up
+  rate_kernel<kKind><<<sms, kThreads, smem>>>(0.5f, cyc, sink);
+  if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return -1.0;
+  std::vector<unsigned long long> h(sms);
+  cudaMemcpy(h.data(), cyc, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost);
+  cudaFree(cyc);
+  cudaFree(sink);
+  std::vector<double> rates;
+  const double ops = double(kThreads) * kChains * kIters;
+  for (int i = 0; i < sms; ++i) rates.push_back(ops / double(h[i]));
+  std::sort(rates.begin(), rates.end());
+  return rates[sms / 2];
+}
+
+int main() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 2;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const double ex2_rate = measure<0>(sms);
+  const double e4m3_rate = measure<1>(sms);
+  const double bf16_rate = measure<2>(sms);
+  if (ex2_rate < 0 || e4m3_rate < 0 || bf16_rate < 0) return 3;
+  printf("{\"sms\": %d, \"ex2_approx_f32_per_clk_sm\": %.2f, "
+         "\"cvt_e4m3x2_f32_instr_per_clk_sm\": %.2f, \"cvt_bf16x2_f32_instr_per_clk_sm\": %.2f}\n",
+         sms, ex2_rate, e4m3_rate, bf16_rate);
+  return 0;
+}

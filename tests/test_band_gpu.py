@@ -45,6 +45,7 @@ def run_and_check(B, H, N, D, dtype, causal, window, slopes=None, modes=(False, 
     ref = oracle.attention(inputs["q"], inputs["k"], inputs["v"], w.scale, causal,
                            dout=inputs["do"], window=window, alibi_slopes=slopes)
     err_o = U.o_err(o.float().cpu().numpy(), ref["o"], dtype)
+    print(f"[parity] {w.describe()} window {window} alibi {slopes is not None}: O raw {err_o:.3e}")
     err_l = U.max_abs(lse.cpu().numpy(), ref["lse"])
     assert err_o <= U.TOL_O, f"O error {err_o:.3e}"
     assert err_l <= U.TOL_LSE, f"LSE error {err_l:.3e}"

@@ -61,6 +61,7 @@ def run_and_check(B, H, N, D, dtype, causal, mask, window=(-1, -1), slopes=None,
                            dout=inputs["do"], window=window, alibi_slopes=slopes,
                            block_mask=mask, block=128)
     err_o = U.o_err(o.float().cpu().numpy(), ref["o"], dtype)
+    print(f"[parity] {w.describe()} block mask, window {window} alibi {slopes is not None}: O raw {err_o:.3e}")
     assert err_o <= U.TOL_O, f"O error {err_o:.3e}"
     check_lse(lse.cpu().numpy(), ref["lse"])
     for det in modes:

@@ -77,6 +77,36 @@ def test_edge_shapes_forward_and_backward(B, H, N, D, dtype, causal):
     U.assert_no_device_error()
 
 
+# Causal shapes whose streamed operands exceed the 64 MiB under which the
+# kernels order their grids tile-major: these run head-major in the forward,
+# the dK/dV kernel (both modes) and the deterministic dQ kernel, the order the
+# long-sequence workload takes, and are small enough for full parity.
+HEAD_MAJOR = [
+    (1, 20, 8192, 128),
+    (1, 40, 8192, 64),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D", HEAD_MAJOR)
+def test_head_major_causal_full_parity(B, H, N, D):
+    # 2 B H N D 16-bit bytes of K and V (forward), 4 B H N D bytes of fp32
+    # (deterministic backward): both above the 64 MiB threshold
+    assert 4 * B * H * N * D > 64 << 20
+    w = W.custom(B, H, N, D, causal=True, seed=N + H)
+    inputs = W.make_inputs(w)
+    g = U.gpu_inputs(w, inputs)
+    o, lse = U.run_forward(w, g)
+    torch.cuda.synchronize()
+    U.check_forward(w, inputs, o, lse)
+    for det in (False, True):
+        dq, dk, dv = U.run_backward(w, g, o, lse, det)
+        torch.cuda.synchronize()
+        errs = U.check_backward_full(w, inputs, dq, dk, dv)
+        print(f"[parity] {w.describe()} {'deterministic' if det else 'atomic'} backward: " +
+              ", ".join(f"{k} {v:.3e}" for k, v in errs.items()))
+    U.assert_no_device_error()
+
+
 @pytest.mark.parametrize("scale", [0.0, -0.2, 0.9])
 def test_forward_scale_edge_cases(scale):
     """scale 0 makes every visible key equally likely; a negative scale
