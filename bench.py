@@ -279,11 +279,12 @@ def block_pairs(N: int, causal: bool, mask) -> int:
     return int((full * (np.asarray(mask) != 0)).sum())
 
 
-def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
-    """Forward + backward (atomic dQ) on the benchmark inputs with a sliding
-    window, with ALiBi, and with a random block mask keeping half the blocks
-    (and the diagonal), credited with the FLOPs of the visible pairs only
-    (4 D per pair forward, 2.5 times that backward)."""
+def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk, det=False):
+    """Forward + backward (the run's dQ mode, whose workspace `ws` is) on the
+    benchmark inputs with a sliding window, with ALiBi, and with a random
+    block mask keeping half the blocks (and the diagonal), credited with the
+    FLOPs of the visible pairs only (4 D per pair forward, 2.5 times that
+    backward)."""
     import torch
 
     from exact_attention_93_gb300 import fattn
@@ -310,7 +311,7 @@ def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
             fattn.fa_fwd_ex(g["q"], g["k"], g["v"], o, lse, None, opts, B, H, N, D, w.scale,
                             w.causal)
             fattn.fa_bwd_ex(g["q"], g["k"], g["v"], o, lse, g["do"], dq, dk, dv, None, opts,
-                            B, H, N, D, w.scale, w.causal, False, ws)
+                            B, H, N, D, w.scale, w.causal, det, ws)
 
         for _ in range(3):
             one()
@@ -328,7 +329,8 @@ def band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk):
         tf = flops / (ms * 1e-3) / 1e12
         out[f"{w.describe()} fwd+bwd, {label}"] = {
             "tflops": tf, "ms": ms, "frac_of_peak": tf / pk["sustained"],
-            "note": "FLOPs of the visible (query, key) pairs only; fa_fwd_ex + fa_bwd_ex"}
+            "note": "FLOPs of the visible (query, key) pairs only; fa_fwd_ex + fa_bwd_ex"
+                    + (" (deterministic dQ)" if det else " (atomic dQ)")}
     if fattn.fa_device_error() != fattn.FA_OK:
         raise RuntimeError("a kernel reported a timed-out wait in the band runs")
     return out
@@ -770,7 +772,7 @@ def run_ours(args, w):
         extra[w2.describe() + " fwd"] = {"tflops": tf2, "ms": ms2,
                                          "frac_of_burst_peak": tf2 / pk["burst"],
                                          "note": "back-to-back launches; inputs 16.8 MB each fit in L2"}
-        extra.update(band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk))
+        extra.update(band_extras(w, g, o, lse, dq, dk, dv, ws, stream, pk, det))
         extra.update(fp8_extras(w, dev, stream, pk))
         # head dimension 64 at the same sequence length and work (twice the heads)
         extra.update(fp8_extras(W.custom(w.B, 2 * w.H, w.N, 64, causal=w.causal, seed=w.seed,

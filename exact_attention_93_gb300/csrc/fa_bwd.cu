@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 //   TMEM [128b + 64, 128b + 128) buffer b: dP^T of tile i; then, for each
 //                                32-query half, P^T and dS^T packed over it
 //   TMEM [256, 384) dV, [384, 512) dK
-// Two warps issue the products.  The score warp issues S^T, dP^T(i) as soon
+// Two warps issue the products, each running its loop with all 32 lanes (the
+// operands stay warp-uniform) while one elected lane issues every product
+// and commit.  The score warp issues S^T, dP^T(i) as soon
 // as buffer i & 1 is free; the gradient warp, once tile i's P^T / dS^T are
 // in TMEM, issues dQ^T(i-1) and then dV, dK(i).  Any stall of an issuing
 // thread (even a wait on a barrier that has already completed) leaves the
@@ -263,7 +265,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ score products
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
+      auto leader_commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
@@ -278,25 +284,29 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
           const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-          tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
+          if (leader) tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
                     desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
           const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-          tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
+          if (leader) tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
                     desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s.s_full[b]);
+        leader_commit(&s.s_full[b]);
       }
-      tc_commit(&s.drain[0]);
+      leader_commit(&s.drain[0]);
       int zero = 0;
       mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp == 14) {
     // ------------------------------------------------------------ gradient products
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
+      auto leader_commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
       // d x queries, over keys; M = 128 at D = 64 too (rows past D unused)
       constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
@@ -307,11 +317,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tbase + ((j + 1) & 1) * 128,
+          if (leader) tc_mma_ss(tbase + ((j + 1) & 1) * 128,
                     desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
                     desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
                     kk > 0 ? 1u : 0u);
-        tc_commit(&s.dq_full[j % 3]);
+        leader_commit(&s.dq_full[j % 3]);
       };
       for (int it = 0; it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
@@ -338,20 +348,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < kQ64 / 16; ++kk)
-          tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+          if (leader) tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
                     desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                     (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
 #pragma unroll
         for (int kk = 0; kk < kQ64 / 16; ++kk)
-          tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+          if (leader) tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
                     desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                     (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&s.qdo_empty[st]);
+        leader_commit(&s.qdo_empty[st]);
         // dV, dK(it) done frees buffer b for tile it + 2: the commit arrives
         // on buf_ready(it + 2) itself, so the score warp wakes on the tensor
         // core's arrival, not on a relay.
-        tc_commit(&s.buf_ready[b]);
+        leader_commit(&s.buf_ready[b]);
       }
       // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
       // has left it and the last dS^T is in shared memory.
@@ -366,8 +376,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
       // The score products all completed before the last P^T / dS^T existed,
       // so this commit covers every product of the CTA.
-      tc_commit(&s.all_done);
-      tc_commit(&s.drain[1]);
+      leader_commit(&s.all_done);
+      leader_commit(&s.drain[1]);
       int zero = 0;
       mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
     }
@@ -634,7 +644,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 // The score warp issues S = Q K^T and dP = dO V^T of tile i once buffer
 // i & 1 is free (dQ(i - 2), the last reader of its dS, done; K, V(i)
 // landed, confirmed by a relay warp so the issuing thread waits once per
-// tile); eight warps form dS = P (dP - Di), P = 2^(S * scale * log2 e -
+// tile; the two issuing warps run their loops whole, one elected lane
+// issuing, and poll their barriers rather than sleep); eight warps form
+// dS = P (dP - Di), P = 2^(S * scale * log2 e -
 // LSE2), one query row per thread so its LSE and Di sit in registers; the
 // gradient warp issues dQ += dS K with dS read from TMEM.  Q and dO are
 // loaded once; K and V come through a three-stage ring.
@@ -764,60 +776,68 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ score products
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
+      auto leader_commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       constexpr uint32_t idS = idesc_f16(128, kK64, ab, 0, 0);  // queries x keys, over d
       const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
-      bool ok = mbar_wait(&s.q_full, 0, p.err, abort_flag);
+      bool ok = mbar_wait_poll(&s.q_full, 0, p.err, abort_flag);
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
-        if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        if (!mbar_wait_poll(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]), v_addr = smem_u32(s.v[st]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
           const uint32_t ok_ = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-          tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(q_addr, 16, 1024), oq),
+          if (leader) tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(q_addr, 16, 1024), oq),
                     desc_add(smem_desc_sw128(k_addr, 16, 1024), ok_), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
           const uint32_t ok_ = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-          tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(do_addr, 16, 1024), oq),
+          if (leader) tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(do_addr, 16, 1024), oq),
                     desc_add(smem_desc_sw128(v_addr, 16, 1024), ok_), idS, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s.s_full[b]);
+        leader_commit(&s.s_full[b]);
       }
-      tc_commit(&s.drain[0]);
+      leader_commit(&s.drain[0]);
       int zero = 0;
-      mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
+      mbar_wait_poll(&s.drain[0], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ gradient products
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
+      auto leader_commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       constexpr uint32_t idQ = idesc_f16(128, D, ab, 0, 1);  // queries x d, over keys
       for (int it = 0; it < n_it; ++it) {
         const int b = it & 1, st = it % 3;
-        if (!mbar_wait(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        if (!mbar_wait_poll(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]);
         // dQ += dS K : A = dS packed in TMEM over the dP columns (keys 32h ..
         // 32h + 31 in columns 32h .. 32h + 15), B = K MN-major (d contiguous)
 #pragma unroll
         for (int kk = 0; kk < kK64 / 16; ++kk)
-          tc_mma_ts(tdQ, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+          if (leader) tc_mma_ts(tdQ, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
                     desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
                     (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&s.kv_empty[st]);  // S, dP(it) completed before dS(it) existed
-        tc_commit(&s.buf_ready[b]);  // frees buffer b for tile it + 2
+        leader_commit(&s.kv_empty[st]);  // S, dP(it) completed before dS(it) existed
+        leader_commit(&s.buf_ready[b]);  // frees buffer b for tile it + 2
       }
       // The score products all completed before the last dS existed, so
       // this commit covers every product of the CTA.
-      tc_commit(&s.all_done);
-      tc_commit(&s.drain[1]);
+      leader_commit(&s.all_done);
+      leader_commit(&s.drain[1]);
       int zero = 0;
-      mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
+      mbar_wait_poll(&s.drain[1], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ elementwise

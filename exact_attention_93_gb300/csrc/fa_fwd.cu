@@ -19,7 +19,10 @@
 //   warp 8     TMA producer: a unit's two Q tiles once (into one of two
 //              buffer sets when the CTA runs several units), K and V tiles
 //              into two smem stages.
-//   warp 9     MMA issuer (one thread).  For key tile j it issues
+//   warp 9     MMA issuer: with 16-bit operands the whole warp runs the
+//              issue loop, so that its operands stay warp-uniform, and one
+//              elected lane issues each product and commit (8-bit operands:
+//              lane 0 alone).  For key tile j it issues
 //                O_A += P_A(j) V_j, S_A(j+1) = Q_A K_{j+1}^T,
 //                O_B += P_B(j) V_j, S_B(j+1) = Q_B K_{j+1}^T,
 //              so while one group's softmax works on its scores the tensor
@@ -361,7 +364,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // 16-bit operands: every lane computes the same descriptors and waits
+    // on the same barriers; only the elected lane issues.  (A single-lane
+    // branch made each product's operands per-thread values to be moved into
+    // uniform registers first: issuing a group's sixteen products then took
+    // longer than the tensor core took to run them.)  8-bit operands keep
+    // the single-lane loop.
+    if (!kFp8 || lane == 0) {
+      const bool leader = kFp8 ? true : elect_one_sync();
+      auto leader_commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       constexpr uint32_t ab = kBf16 ? 1u : 0u;
       constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, ab, 0, 0);
       // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
@@ -401,12 +414,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
           for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
             const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-            mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
+            if (leader) mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
                          kk > 0 ? 1u : 0u);
           }
-          tc_commit(&s.s_full[t]);
+          leader_commit(&s.s_full[t]);
           if constexpr (kResident)
-            if (--s_left == 0) tc_commit(&s.q_empty[qs]);
+            if (--s_left == 0) leader_commit(&s.q_empty[qs]);
         };
         const int jf = walk.first();
         // with nothing to multiply (an empty block-sparse pair) no K arrives
@@ -414,13 +427,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                   (jf >= walk.n || mbar_wait_poll(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
         if (!ok) return false;
         if (jf >= walk.n) {
-          if constexpr (kResident) tc_commit(&s.q_empty[qs]);
+          if constexpr (kResident) leader_commit(&s.q_empty[qs]);
           return true;
         }
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (walk.has(t, jf)) issue_s(t, kv & 1);
-        tc_commit(&s.k_empty[kv & 1]);
+        leader_commit(&s.k_empty[kv & 1]);
         int n_stream = 0;  // key tiles in this unit's K/V stream
         if constexpr (!kSparse) {
           // dense: each tile's key tiles are the range [lo_t, hi_t]
@@ -451,9 +464,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                  mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                  if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
                                idPV, (j > lt || kk > 0) ? 1u : 0u);
-                tc_commit(&s.o_done[t]);
+                leader_commit(&s.o_done[t]);
               }
               if (s_next) {
                 if (!k_next) {
@@ -468,8 +481,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
               }
             }
-            tc_commit(&s.v_empty[st]);
-            if (k_next) tc_commit(&s.k_empty[(g + 1) & 1]);
+            leader_commit(&s.v_empty[st]);
+            if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
           }
           n_stream = j_last - j_first + 1;
         } else {
@@ -500,9 +513,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                  mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                  if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
                                idPV, (ct > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&s.o_done[t]);
+                leader_commit(&s.o_done[t]);
                 if (t)
                   ++c1;
                 else
@@ -521,8 +534,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
               }
             }
-            tc_commit(&s.v_empty[st]);
-            if (k_next) tc_commit(&s.k_empty[(g + 1) & 1]);
+            leader_commit(&s.v_empty[st]);
+            if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
           }
         }
         kv_run = kv + static_cast<uint32_t>(n_stream);
@@ -531,7 +544,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         return ok;
       });
       // Every MMA issued above completes before TMEM is released.
-      tc_commit(&s.drain);
+      leader_commit(&s.drain);
       int zero = 0;
       mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
     }

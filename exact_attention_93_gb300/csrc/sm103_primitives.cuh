@@ -85,6 +85,17 @@ __device__ __forceinline__ bool mbar_try_wait_poll(uint64_t* bar, uint32_t parit
   return ok != 0;
 }
 
+// One lane of the (converged) warp: true in exactly one of them.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Longest a single wait may take before the kernel gives up (ns).  Every
 // wait in a healthy launch ends in microseconds.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
