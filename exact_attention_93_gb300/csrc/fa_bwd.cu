@@ -115,16 +115,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 // dK / dV, software-pipelined over 64-row query tiles (D = 64 or 128)
 // ---------------------------------------------------------------------------
 // With 64-row query tiles the scores and their gradient take 64 TMEM columns
-// each, so two tiles' S^T / dP^T fit beside the dV and dK accumulators:
-//   TMEM [128b, 128b + 64)       buffer b: S^T of tile i (b = i & 1), then
+// each, so NB tiles' S^T / dP^T fit beside the dV and dK accumulators (NB = 2
+// at D = 128, 3 at D = 64):
+//   TMEM [128b, 128b + 64)       buffer b: S^T of tile i (b = i % NB), then
 //                                dQ^T of tile i - 1 once S^T is consumed
 //   TMEM [128b + 64, 128b + 128) buffer b: dP^T of tile i; then, for each
 //                                32-query half, P^T and dS^T packed over it
-//   TMEM [256, 384) dV, [384, 512) dK
+//   TMEM [128 NB, 128 NB + D) dV, [128 NB + D, 128 NB + 2D) dK
 // Two warps issue the products, each running its loop with all 32 lanes (the
 // operands stay warp-uniform) while one elected lane issues every product
 // and commit.  The score warp issues S^T, dP^T(i) as soon
-// as buffer i & 1 is free; the gradient warp, once tile i's P^T / dS^T are
+// as buffer i % NB is free; the gradient warp, once tile i's P^T / dS^T are
 // in TMEM, issues dQ^T(i-1) and then dV, dK(i).  Any stall of an issuing
 // thread (even a wait on a barrier that has already completed) leaves the
 // tensor core idle for a few hundred cycles while its next products travel
@@ -146,22 +147,28 @@ constexpr int kQ64 = 64;
 
 template <int D, bool kSparse>
 struct DkdvPipeSmem {
+  // TMEM buffers for S^T / dP^T: as many as fit beside dV and dK (D = 64:
+  // 3 x 128 + 2 x 64 = 512 columns; D = 128: 2 x 128 + 2 x 128)
+  static constexpr int kBufs = D == 64 ? 3 : 2;
+  // Q / dO stages: one more than the buffers, so that a tile's loads start
+  // before the buffer it will use is free
+  static constexpr int kQStages = kBufs + 1;
   static constexpr int kDBlocks = D / 64;      // 64-column blocks of a row
   static constexpr int kKBlock = kTile * 128;  // 128 rows x 128 B
   static constexpr int kQBlock = kQ64 * 128;   // 64 rows x 128 B
   alignas(1024) uint8_t k[kDBlocks * kKBlock];     // [D block][128 keys][64 d]
   alignas(1024) uint8_t v[kDBlocks * kKBlock];
-  alignas(1024) uint8_t q[3][kDBlocks * kQBlock];  // [stage][D block][64 queries][64 d]
-  alignas(1024) uint8_t dO[3][kDBlocks * kQBlock];
+  alignas(1024) uint8_t q[kQStages][kDBlocks * kQBlock];  // [stage][D block][64 queries][64 d]
+  alignas(1024) uint8_t dO[kQStages][kDBlocks * kQBlock];
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
-  alignas(16) float lse2[3][kQ64];
-  alignas(16) float di[3][kQ64];
+  alignas(16) float lse2[kQStages][kQ64];
+  alignas(16) float di[kQStages][kQ64];
   // D = 64, atomic mode: drained dQ tiles [64 queries][D] for the bulk
   // reductions, double-buffered
   alignas(1024) float dq_stage[D == 64 ? 2 : 1][D == 64 ? kQ64 * D : 1];
-  uint64_t kv_full, qdo_full[3], qdo_empty[3], s_full[2], s_read[2], p_full[2];
-  uint64_t buf_ready[2];
-  uint64_t dq_full[3], tmem_free[2], ds_last, all_done, drain[2];
+  uint64_t kv_full, qdo_full[kQStages], qdo_empty[kQStages], s_full[kBufs], s_read[kBufs], p_full[kBufs];
+  uint64_t buf_ready[kBufs];
+  uint64_t dq_full[3], tmem_free[kBufs], ds_last, all_done, drain[2];
   uint64_t stage_full[2], stage_free[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -173,6 +180,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     bwd_dkdv_pipe_kernel(const __grid_constant__ BwdLaunch p) {
   using Smem = DkdvPipeSmem<D, kSparse>;
   constexpr int kDB = Smem::kDBlocks;
+  constexpr int kNB = Smem::kBufs;  // S^T / dP^T buffers: tile it uses buffer it % kNB
+  constexpr int kQS = Smem::kQStages;  // Q / dO stages: tile it uses stage it % kQS
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -200,18 +209,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 
   if (tid == 0) {
     mbar_init(&s.kv_full, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kQS; ++i) {
       mbar_init(&s.qdo_full[i], 1);
       mbar_init(&s.qdo_empty[i], 1);
-      mbar_init(&s.dq_full[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) mbar_init(&s.dq_full[i], 1);
+    for (int i = 0; i < kNB; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
       mbar_init(&s.s_read[i], 8);  // one arrival per elementwise warp
-      // four buffer warps and the tcgen05.commit that retires dV, dK(it - 2)
+      // four buffer warps and the tcgen05.commit that retires dV, dK(it - kNB)
       mbar_init(&s.buf_ready[i], 5);
       mbar_init(&s.tmem_free[i], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.drain[i], 1);
       mbar_init(&s.stage_full[i], 2);  // the two buffer warps holding dQ rows d < 64
       mbar_init(&s.stage_free[i], 1);  // the thread that issues the reductions
@@ -229,7 +240,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tdV = tbase + 256, tdK = tbase + 384;
+  const uint32_t tdV = tbase + kNB * 128, tdK = tdV + D;
   volatile int* abort_flag = &s.abort_flag;
   constexpr uint32_t ab = kBf16 ? 1u : 0u;
 
@@ -243,8 +254,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       }
       int issued = 0;
       for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-        const int st = it % 3;
-        if (it >= 3 && !mbar_wait(&s.qdo_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
+        const int st = it % kQS;
+        if (it >= kQS && !mbar_wait(&s.qdo_empty[st], ((it - kQS) / kQS) & 1, p.err, abort_flag))
+          break;
         const int q0 = qt * kQ64;
         mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
         for (int kb = 0; kb < kDB; ++kb) {
@@ -259,8 +271,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       if (*abort_flag) {
         int zero = 0;
         mbar_wait(&s.kv_full, 0, p.err, &zero, 100000000ull);
-        for (int t = max(0, issued - 3); t < issued; ++t)
-          mbar_wait(&s.qdo_full[t % 3], (t / 3) & 1, p.err, &zero, 100000000ull);
+        for (int t = max(0, issued - kQS); t < issued; ++t)
+          mbar_wait(&s.qdo_full[t % kQS], (t / kQS) & 1, p.err, &zero, 100000000ull);
       }
     }
   } else if (warp == 13) {
@@ -274,10 +286,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
       bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
       for (int it = 0; ok && it < n_it; ++it) {
-        const int b = it & 1, st = it % 3;
+        const int b = it % kNB, st = it % kQS;
         // Buffer b may take tile it once buf_ready(it) completes: one wait
         // here instead of three (each wait of this thread costs tensor time).
-        if (!mbar_wait(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        if (!mbar_wait(&s.buf_ready[b], (it / kNB) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
 #pragma unroll
@@ -312,34 +324,34 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
       const uint32_t k_addr = smem_u32(s.k);
       bool ok = true;
-      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) & 1.
+      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) % kNB.
       auto issue_dq = [&](int j) {
         const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          if (leader) tc_mma_ss(tbase + ((j + 1) & 1) * 128,
+          if (leader) tc_mma_ss(tbase + ((j + 1) % kNB) * 128,
                     desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
                     desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
                     kk > 0 ? 1u : 0u);
         leader_commit(&s.dq_full[j % 3]);
       };
       for (int it = 0; it < n_it; ++it) {
-        const int b = it & 1, st = it % 3;
+        const int b = it % kNB, st = it % kQS;
         if (kAtomicDq && it >= 1) {
           // S^T(it) is in the elementwise warps' registers: dQ^T(it - 1) can
-          // take its columns (their previous occupant, dQ^T(it - 3), was
+          // take its columns (their previous occupant, dQ^T(it - 1 - kNB), was
           // drained before S^T(it) was issued), and dS^T(it - 1) reached
           // shared memory before that signal.  It runs while the
           // elementwise step of tile it does, off the chain that frees
           // buffer b for S^T(it + 2).
-          if (!mbar_wait(&s.s_read[b], (it >> 1) & 1, p.err, abort_flag)) {
+          if (!mbar_wait(&s.s_read[b], (it / kNB) & 1, p.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_dq(it - 1);
         }
-        if (!mbar_wait(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) {
+        if (!mbar_wait(&s.p_full[b], (it / kNB) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -358,18 +370,18 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
                     (it > 0 || kk > 0) ? 1u : 0u);
         leader_commit(&s.qdo_empty[st]);
-        // dV, dK(it) done frees buffer b for tile it + 2: the commit arrives
-        // on buf_ready(it + 2) itself, so the score warp wakes on the tensor
-        // core's arrival, not on a relay.
+        // dV, dK(it) done frees buffer b for tile it + kNB: the commit
+        // arrives on buf_ready(it + kNB) itself, so the score warp wakes on
+        // the tensor core's arrival, not on a relay.
         leader_commit(&s.buf_ready[b]);
       }
-      // The last tile's dQ^T goes into buffer n_it & 1, once dQ^T(n_it - 3)
-      // has left it and the last dS^T is in shared memory.
+      // The last tile's dQ^T goes into buffer n_it % kNB, once
+      // dQ^T(n_it - 1 - kNB) has left it and the last dS^T is in shared memory.
       if (ok && kAtomicDq && !*abort_flag && n_it > 0) {
         const int j = n_it - 1;
         if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
-            (j < 2 ||
-             mbar_wait(&s.tmem_free[(j + 1) & 1], ((j - 2) >> 1) & 1, p.err, abort_flag))) {
+            (j < kNB || mbar_wait(&s.tmem_free[(j + 1) % kNB], ((j - kNB) / kNB) & 1, p.err,
+                                  abort_flag))) {
           tc_fence_after();
           issue_dq(j);
         }
@@ -383,9 +395,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ buffer warps
-    // Buffer it & 1 may take S^T, dP^T(it) once dV, dK(it - 2) are done (the
-    // last readers of its P^T / dS^T; their tcgen05.commit arrives on
-    // buf_ready(it) directly), dQ^T(it - 3) has left its S^T columns (atomic
+    // Buffer it % kNB may take S^T, dP^T(it) once dV, dK(it - kNB) are done
+    // (the last readers of its P^T / dS^T; their tcgen05.commit arrives on
+    // buf_ready(it) directly), dQ^T(it - 1 - kNB) has left its S^T columns (atomic
     // mode) and Q / dO(it) have landed.  These warps see to the last two,
     // arrive on buf_ready(it), and in atomic mode drain dQ^T (TMEM lane =
     // column d of dQ) into the fp32 accumulator.
@@ -393,9 +405,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const int d = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     int qt_dq = walk.first();  // query tile of the dQ^T drained next
-    for (int it = 0; it < n_it + (kAtomicDq ? 3 : 0); ++it) {
-      const int b = it & 1;
-      const int j = it - 3;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) & 1 = b
+    for (int it = 0; it < n_it + (kAtomicDq ? kNB + 1 : 0); ++it) {
+      const int b = it % kNB;
+      const int j = it - 1 - kNB;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) % kNB = b
       const bool drain = kAtomicDq && j >= 0 && j < n_it;
       uint32_t g[2][32];
       if (drain) {
@@ -408,12 +420,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         mbar_arrive(&s.tmem_free[b]);  // for the last tile's dQ^T
       }
       if (it < n_it) {
-        if (!warp_wait(&s.qdo_full[it % 3], (it / 3) & 1, p.err, abort_flag)) break;
+        if (!warp_wait(&s.qdo_full[it % kQS], (it / kQS) & 1, p.err, abort_flag)) break;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&s.buf_ready[b]);
-          // tiles 0 and 1 have no dV, dK(it - 2) to wait for
-          if (it < 2 && warp == 8) mbar_arrive(&s.buf_ready[b]);
+          // the first kNB tiles have no dV, dK(it - kNB) to wait for
+          if (it < kNB && warp == 8) mbar_arrive(&s.buf_ready[b]);
         }
       }
       if (drain) {
@@ -476,12 +488,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
     bool ok = true;
     for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-      const int b = it & 1, st = it % 3;
+      const int b = it % kNB, st = it % kQS;  // buffer, Q / dO stage
+      const int sd = it % 3;                   // dS^T stage
       const int q0 = qt * kQ64;
-      // S^T(it) was issued after dV, dK(it - 2), the last readers of the
+      // S^T(it) was issued after dV, dK(it - kNB), the last readers of the
       // P^T / dS^T columns of buffer b, had completed.
-      if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag) ||
-          !warp_wait(&s.qdo_full[st], (it / 3) & 1, p.err, abort_flag)) {
+      if (!warp_wait(&s.s_full[b], (it / kNB) & 1, p.err, abort_flag) ||
+          !warp_wait(&s.qdo_full[st], (it / kQS) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
@@ -572,11 +585,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       mbar_arrive(&s.p_full[b]);
       if (kAtomicDq) {
         // dQ^T(it - 3) was the last reader of dS^T buffer it % 3
-        if (it >= 3 && !warp_wait(&s.dq_full[st], ((it - 3) / 3) & 1, p.err, abort_flag)) {
+        if (it >= 3 && !warp_wait(&s.dq_full[sd], ((it - 3) / 3) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        store_row_chunk_sw128(s.dst[st], r, half, dk);
+        store_row_chunk_sw128(s.dst[sd], r, half, dk);
         fence_proxy_async_smem();
       }
     }
@@ -586,7 +599,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
     if (named_bar_and(1, 256, done)) {
       tc_fence_after();
-      // D x 128 keys x 2 B of the free query ring each (16 or 32 KB of 24 or 48)
+      // D x 128 keys x 2 B of the free query ring each (16 or 32 KB of 32 or 48)
       uint8_t* dk_tile = s.q[0];
       uint8_t* dv_tile = s.dO[0];
 #pragma unroll 1
