@@ -650,34 +650,39 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 // ---------------------------------------------------------------------------
 // One CTA per 128-row query tile.  dQ accumulates in TMEM over the key tiles
 // in a fixed order, so the result does not depend on scheduling:
-//   TMEM [128b, 128b + 64)       buffer b: S of key tile i (b = i & 1)
+//   TMEM [128b, 128b + 64)       buffer b: S of key tile i (b = i % 3)
 //   TMEM [128b + 64, 128b + 128) buffer b: dP of tile i, then dS packed over
 //                                each elementwise warp's own 32 columns
-//   TMEM [256, 256 + D)          dQ
+//   TMEM [384, 384 + D)          dQ
 // The score warp issues S = Q K^T and dP = dO V^T of tile i once buffer
-// i & 1 is free (dQ(i - 2), the last reader of its dS, done; K, V(i)
+// i % 3 is free (dQ(i - 3), the last reader of its dS, done; K, V(i)
 // landed, confirmed by a relay warp so the issuing thread waits once per
 // tile; the two issuing warps run their loops whole, one elected lane
 // issuing, and poll their barriers rather than sleep); eight warps form
 // dS = P (dP - Di), P = 2^(S * scale * log2 e -
 // LSE2), one query row per thread so its LSE and Di sit in registers; the
 // gradient warp issues dQ += dS K with dS read from TMEM.  Q and dO are
-// loaded once; K and V come through a three-stage ring.
+// loaded once; K and V come through a four-stage ring.
 constexpr int kDqPipeThreads = 384;  // warps 0-7 elementwise, 8 relay, 9 producer, 10-11 MMA
 constexpr int kK64 = 64;
 
 template <int D, bool kSparse>
 struct DqPipeSmem {
+  // TMEM buffers for S / dP (3 x 128 columns beside dQ's D) and K / V
+  // stages (one more, so that a tile's loads start before its buffer is free)
+  static constexpr int kBufs = 3;
+  static constexpr int kKVStages = kBufs + 1;
   static constexpr int kDBlocks = D / 64;
   static constexpr int kQBlock = kTile * 128;  // 128 rows x 128 B
   static constexpr int kKBlock = kK64 * 128;   // 64 rows x 128 B
   alignas(1024) uint8_t q[kDBlocks * kQBlock];  // [D block][128 queries][64 d]; then dQ
   alignas(1024) uint8_t dO[kDBlocks * kQBlock];
-  alignas(1024) uint8_t k[3][kDBlocks * kKBlock];  // [stage][D block][64 keys][64 d]
-  alignas(1024) uint8_t v[3][kDBlocks * kKBlock];
+  alignas(1024) uint8_t k[kKVStages][kDBlocks * kKBlock];  // [stage][D block][64 keys][64 d]
+  alignas(1024) uint8_t v[kKVStages][kDBlocks * kKBlock];
   alignas(16) float lse2[kTile];
   alignas(16) float di[kTile];
-  uint64_t q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], buf_ready[2];
+  uint64_t q_full, kv_full[kKVStages], kv_empty[kKVStages], s_full[kBufs], p_full[kBufs],
+      buf_ready[kBufs];
   uint64_t all_done, drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -689,6 +694,8 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
     bwd_dq_pipe_kernel(const __grid_constant__ BwdLaunch p) {
   using Smem = DqPipeSmem<D, kSparse>;
   constexpr int kDB = Smem::kDBlocks;
+  constexpr int kNB = Smem::kBufs;       // S / dP buffers: tile it uses buffer it % kNB
+  constexpr int kKS = Smem::kKVStages;   // K / V stages: tile it uses stage it % kKS
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -717,17 +724,17 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kKS; ++i) {
       mbar_init(&s.kv_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNB; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
-      // the relay warp and the tcgen05.commit that retires dQ(it - 2)
+      // the relay warp and the tcgen05.commit that retires dQ(it - kNB)
       mbar_init(&s.buf_ready[i], 2);
-      mbar_init(&s.drain[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&s.drain[i], 1);
     mbar_init(&s.all_done, 1);
     s.abort_flag = 0;
     fence_barrier_init();
@@ -740,7 +747,7 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tdQ = tbase + 256;
+  const uint32_t tdQ = tbase + kNB * 128;
   volatile int* abort_flag = &s.abort_flag;
   constexpr uint32_t ab = kBf16 ? 1u : 0u;
 
@@ -757,8 +764,9 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
       bulk_load(s.di, p.di + off, kTile * 4, &s.q_full);
       int issued = 0;
       for (int it = 0, t = walk.first(); it < n_it; ++it, t = walk.next(t)) {
-        const int st = it % 3;
-        if (it >= 3 && !mbar_wait(&s.kv_empty[st], ((it - 3) / 3) & 1, p.err, abort_flag)) break;
+        const int st = it % kKS;
+        if (it >= kKS && !mbar_wait(&s.kv_empty[st], ((it - kKS) / kKS) & 1, p.err, abort_flag))
+          break;
         mbar_arrive_expect_tx(&s.kv_full[st], 2 * kDB * Smem::kKBlock);
         for (int kb = 0; kb < kDB; ++kb) {
           tma_load_4d(s.k[st] + kb * Smem::kKBlock, &p.map_k64, &s.kv_full[st], kb * 64,
@@ -772,19 +780,19 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
         // Let copies already in flight land before the CTA's smem goes away.
         int zero = 0;
         mbar_wait(&s.q_full, 0, p.err, &zero, 100000000ull);
-        for (int t = max(0, issued - 3); t < issued; ++t)
-          mbar_wait(&s.kv_full[t % 3], (t / 3) & 1, p.err, &zero, 100000000ull);
+        for (int t = max(0, issued - kKS); t < issued; ++t)
+          mbar_wait(&s.kv_full[t % kKS], (t / kKS) & 1, p.err, &zero, 100000000ull);
       }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ relay
-    // Buffer it & 1 takes S, dP(it) once K, V(it) have landed (seen here)
-    // and dQ(it - 2) is done (its tcgen05.commit arrives on buf_ready).
+    // Buffer it % kNB takes S, dP(it) once K, V(it) have landed (seen here)
+    // and dQ(it - kNB) is done (its tcgen05.commit arrives on buf_ready).
     for (int it = 0; it < n_it; ++it) {
-      if (!warp_wait(&s.kv_full[it % 3], (it / 3) & 1, p.err, abort_flag)) break;
+      if (!warp_wait(&s.kv_full[it % kKS], (it / kKS) & 1, p.err, abort_flag)) break;
       if (lane == 0) {
-        mbar_arrive(&s.buf_ready[it & 1]);
-        if (it < 2) mbar_arrive(&s.buf_ready[it & 1]);  // no dQ(it - 2) to wait for
+        mbar_arrive(&s.buf_ready[it % kNB]);
+        if (it < kNB) mbar_arrive(&s.buf_ready[it % kNB]);  // no dQ(it - kNB) to wait for
       }
     }
   } else if (warp == 10) {
@@ -798,8 +806,8 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
       const uint32_t q_addr = smem_u32(s.q), do_addr = smem_u32(s.dO);
       bool ok = mbar_wait_poll(&s.q_full, 0, p.err, abort_flag);
       for (int it = 0; ok && it < n_it; ++it) {
-        const int b = it & 1, st = it % 3;
-        if (!mbar_wait_poll(&s.buf_ready[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        const int b = it % kNB, st = it % kKS;
+        if (!mbar_wait_poll(&s.buf_ready[b], (it / kNB) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]), v_addr = smem_u32(s.v[st]);
 #pragma unroll
@@ -831,8 +839,8 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
       };
       constexpr uint32_t idQ = idesc_f16(128, D, ab, 0, 1);  // queries x d, over keys
       for (int it = 0; it < n_it; ++it) {
-        const int b = it & 1, st = it % 3;
-        if (!mbar_wait_poll(&s.p_full[b], (it >> 1) & 1, p.err, abort_flag)) break;
+        const int b = it % kNB, st = it % kKS;
+        if (!mbar_wait_poll(&s.p_full[b], (it / kNB) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]);
         // dQ += dS K : A = dS packed in TMEM over the dP columns (keys 32h ..
@@ -863,9 +871,9 @@ __global__ void __launch_bounds__(kDqPipeThreads, 1)
     bool ok = warp_wait(&s.q_full, 0, p.err, abort_flag);
     const float lse2 = s.lse2[r], dii = s.di[r];  // +inf / 0 for rows past N
     for (int it = 0, t = walk.first(); ok && it < n_it; ++it, t = walk.next(t)) {
-      const int b = it & 1;
+      const int b = it % kNB;
       const int k0 = t * kK64;
-      if (!warp_wait(&s.s_full[b], (it >> 1) & 1, p.err, abort_flag)) {
+      if (!warp_wait(&s.s_full[b], (it / kNB) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
