@@ -748,7 +748,10 @@ def run_ours(args, w):
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H results
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, w, inputs, dev, det, dist, world, fwd_f + bwd_alg)
+        with ClockSampler(local) as clk_e2e:
+            e2e = measure_e2e(args, w, inputs, dev, det, dist, world, fwd_f + bwd_alg)
+        # the clocks while copies and compute overlap (power draw is higher)
+        e2e["clocks"] = clk_e2e.summary()
 
     # the long-context forward-only workload, reported beside the step
     extra = {}

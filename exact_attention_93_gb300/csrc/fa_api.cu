@@ -17,15 +17,19 @@ __device__ uint32_t g_error_word;  // written by bounded waits that run out
 constexpr int kMaxDevices = 64;
 
 uint32_t* error_word_ptr() {
+  // resolved once per device and context (a cudaDeviceReset makes a new one)
   static uint32_t* ptrs[kMaxDevices] = {};
+  static CUcontext ctxs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || ctxs[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<uint32_t*>(p);
+    ctxs[dev] = ctx;
   }
   return ptrs[dev];
 }

@@ -29,18 +29,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 
 // Device address of g_noalloc_scratch on the current device (set up on the
-// first call per device); nullptr if it cannot be resolved.
+// first call per device, and again on the first call after the device's
+// context was replaced, e.g. by cudaDeviceReset); nullptr if it cannot be
+// resolved.
 unsigned char* scratch_ptr() {
   static unsigned char* ptrs[kMaxDevices] = {};
+  static CUcontext ctxs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || ctxs[dev] != ctx) {
     unsigned char* p = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess)
       return nullptr;
     ptrs[dev] = p;
+    ctxs[dev] = ctx;
   }
   return ptrs[dev];
 }

@@ -308,6 +308,9 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int D, float scale, f
  *     anything is enqueued (B*H*ceil(N/128)*128 may be at most 2^20 rows).
  *   - The first call on a device resolves the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     A cudaDeviceReset replaces the device's context and with it that
+ *     address: the first call after it resolves the address again (so it,
+ *     too, should come before any capture).
  *   - Every call on a device shares the one array, and each call overwrites
  *     it completely.  Calls whose work can overlap on the GPU (different
  *     streams, no ordering between them) race on it: order them on one stream.
