@@ -584,7 +584,10 @@ def measure_e2e(args, w, inputs, dev, det, dist, world, flops):
         fattn.fa_bwd(g["q"], g["k"], g["v"], S["o"], S["lse"], g["do"], S["dq"], S["dk"],
                      S["dv"], w.scale, w.causal, det, S["ws"])
 
+    comp_ev = []  # (start, end) of each step's compute on its stream
+
     def run(steps, start=None, end=None):
+        comp_ev.clear()
         if start is not None:
             start.record(s_in)
         for k in range(steps):
@@ -600,7 +603,11 @@ def measure_e2e(args, w, inputs, dev, det, dist, world, flops):
             if k >= 2:
                 s_comp.wait_event(ev["out"][b])  # step k - 2's results have left set b
             with torch.cuda.stream(s_comp):
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(s_comp)
                 compute(S)
+                c1.record(s_comp)
+                comp_ev.append((c0, c1))
                 ev["comp"][b].record(s_comp)
             s_out.wait_event(ev["comp"][b])
             with torch.cuda.stream(s_out):
@@ -620,6 +627,8 @@ def measure_e2e(args, w, inputs, dev, det, dist, world, flops):
     run(args.steps, s2, e2)
     torch.cuda.synchronize()
     e_ms = slowest_rank(s2.elapsed_time(e2) / args.steps, dist, dev)
+    # the compute alone inside that loop (while the copies run beside it)
+    comp_ms = statistics.median(a.elapsed_time(b) for a, b in comp_ev)
 
     # the copies alone, for context (outside the timed region)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -640,6 +649,7 @@ def measure_e2e(args, w, inputs, dev, det, dist, world, flops):
     return {"value": whole_job_tflops(world, flops, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_gbps_alone": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbps_alone": d2h / (d2h_ms * 1e-3) / 1e9,
+            "compute_ms_per_step_in_loop": comp_ms,
             "pipeline": "copies on their own streams, double-buffered: step k+1's inputs and step "
                         "k-1's results travel while step k computes"}
 
