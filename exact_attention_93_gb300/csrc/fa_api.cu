@@ -19,11 +19,11 @@ constexpr int kMaxDevices = 64;
 uint32_t* error_word_ptr() {
   // resolved once per device and context (a cudaDeviceReset makes a new one)
   static uint32_t* ptrs[kMaxDevices] = {};
-  static CUcontext ctxs[kMaxDevices] = {};
+  static unsigned long long ctxs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  const CUcontext ctx = current_context();
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev] || ctxs[dev] != ctx) {
     void* p = nullptr;

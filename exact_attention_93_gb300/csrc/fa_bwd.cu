@@ -1035,7 +1035,7 @@ template <int D, bool kBf16, bool kAlibi, bool kSparse>
 cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   auto kern = bwd_dq_pipe_kernel<D, kBf16, kAlibi, kSparse>;
   const int smem = static_cast<int>(sizeof(DqPipeSmem<D, kSparse>)) + 1024;
-  static std::atomic<uint64_t> configured{0};
+  static AttrCache configured;
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
@@ -1050,7 +1050,7 @@ template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
 cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
   auto kern = bwd_dkdv_pipe_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
   const int smem = static_cast<int>(sizeof(DkdvPipeSmem<D, kSparse>)) + 1024;
-  static std::atomic<uint64_t> configured{0};
+  static AttrCache configured;
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;

@@ -839,7 +839,7 @@ template <int D, bool kBf16, bool kAlibi, bool kSparse, bool kFp8, bool kResiden
 cudaError_t launch_fwd_grid(const FwdLaunch& b, long long grid, cudaStream_t stream) {
   auto kern = fa_fwd_kernel<D, kBf16, kAlibi, kSparse, kFp8, kResident>;
   const int smem = static_cast<int>(sizeof(FwdSmem<D, kSparse, kFp8>)) + 1024;
-  static std::atomic<uint64_t> configured{0};
+  static AttrCache configured;
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(b);

@@ -3,27 +3,74 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 namespace fa {
 
+// A process-unique ID of the calling thread's current CUDA context (0 if
+// there is none or the driver entry points are unavailable), fetched through
+// the runtime's entry-point query so that the library does not link against
+// libcuda.  What the library caches per device (device addresses of its
+// globals, function attributes) is tagged with it: a cudaDeviceReset
+// destroys the context those belong to, and the next call then sets them up
+// again.  (The ID, unlike the context's handle, is never reused.)
+inline unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// The contexts (IDs, one per device) in which a kernel's attribute was set.
+struct AttrCache {
+  std::mutex mu;
+  unsigned long long ctx[64] = {};
+};
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
-// device, once per device: the attribute belongs to the function as loaded
-// on each device, so a process that drives several GPUs sets it on each.
-// `done` is the calling launcher's own bitmask of devices already set
-// (devices past 63 are set on every call).
+// device, once per device and context: the attribute belongs to the function
+// as loaded in each context, so a process that drives several GPUs sets it
+// on each, and again after a cudaDeviceReset.  `cache` is the calling
+// launcher's own record (devices past 63 are set on every call).
 template <typename K>
-cudaError_t ensure_dynamic_smem(K kern, int bytes, std::atomic<uint64_t>& done) {
+cudaError_t ensure_dynamic_smem(K kern, int bytes, AttrCache& cache) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
-  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const bool tracked = dev >= 0 && dev < 64;
+  const unsigned long long ctx = current_context_id();
+  if (tracked && ctx != 0) {
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (cache.ctx[dev] == ctx) return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  if (e == cudaSuccess && tracked && ctx != 0) {
+    std::lock_guard<std::mutex> lock(cache.mu);
+    cache.ctx[dev] = ctx;
+  }
   return e;
 }
 

@@ -34,11 +34,11 @@ constexpr int kMaxDevices = 64;
 // resolved.
 unsigned char* scratch_ptr() {
   static unsigned char* ptrs[kMaxDevices] = {};
-  static CUcontext ctxs[kMaxDevices] = {};
+  static unsigned long long ctxs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  const CUcontext ctx = current_context();
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev] || ctxs[dev] != ctx) {
     unsigned char* p = nullptr;

@@ -28,26 +28,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The calling thread's current CUDA context (nullptr if none or if the
-// driver entry point is unavailable).  Device addresses the library caches
-// per device are tagged with it: a cudaDeviceReset destroys the context the
-// addresses belong to, and the next call then resolves them again.
-inline CUcontext current_context() {
-  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-  });
-  CUcontext ctx = nullptr;
-  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
-  return ctx;
-}
-
 // A [batch][head][rows][inner] tensor of elem_bytes-byte elements with
 // arbitrary element strides for rows, heads and batches (inner contiguous).
 // Boxes are box_inner x box_rows x 1 x 1; out-of-range rows (and inner

@@ -2,7 +2,10 @@
 compiles against include/fattn.h and links against libfattn.so and the CUDA
 runtime alone (CPU test); on the GPU it runs the forward and the
 deterministic backward on buffers it allocates itself, and its outputs match
-the oracle (GPU test)."""
+the oracle (GPU test).  A second program (tests/c_abi/fa_c_reset.c) runs the
+forward and the no-allocation backward, resets the device, and runs them
+again: what the library set up once per device must be set up again in the
+new context, and the outputs must be identical."""
 import os
 import subprocess
 
@@ -17,14 +20,15 @@ from exact_attention_93_gb300 import build, fattn, workloads as W
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "c_abi", "fa_c_example.c")
+RESET_SRC = os.path.join(HERE, "c_abi", "fa_c_reset.c")
 CUDA = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
-def compile_example(out_dir):
+def compile_example(out_dir, src=SRC, name="fa_c_example"):
     build.build()
-    exe = os.path.join(out_dir, "fa_c_example")
+    exe = os.path.join(out_dir, name)
     lib_dir = os.path.dirname(fattn.LIB_PATH)
-    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-Werror", SRC,
+    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-Werror", src,
                     "-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include"),
                     "-L", lib_dir, "-lfattn", "-L", os.path.join(CUDA, "lib64"), "-lcudart",
                     f"-Wl,-rpath,{lib_dir}", f"-Wl,-rpath,{os.path.join(CUDA, 'lib64')}",
@@ -34,6 +38,15 @@ def compile_example(out_dir):
 
 def test_example_compiles_and_links(tmp_path):
     assert os.path.exists(compile_example(str(tmp_path)))
+    assert os.path.exists(compile_example(str(tmp_path), RESET_SRC, "fa_c_reset"))
+
+
+@pytest.mark.gpu
+def test_outputs_identical_across_a_device_reset(tmp_path):
+    exe = compile_example(str(tmp_path), RESET_SRC, "fa_c_reset")
+    r = subprocess.run([exe, "1", "2", "300", "64", "1"], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
 
 
 @pytest.mark.gpu
