@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 constexpr int kPipeThreads = 480;  // warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA
 constexpr int kQ64 = 64;
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kResident>
 struct DkdvPipeSmem {
   // TMEM buffers for S^T / dP^T: as many as fit beside dV and dK (D = 64:
   // 3 x 128 + 2 x 64 = 512 columns; D = 128: 2 x 128 + 2 x 128)
@@ -153,11 +153,13 @@ struct DkdvPipeSmem {
   // Q / dO stages: one more than the buffers, so that a tile's loads start
   // before the buffer it will use is free
   static constexpr int kQStages = kBufs + 1;
+  // K / V buffers: a resident CTA loads its next key tile's while this one runs
+  static constexpr int kKVBufs = kResident ? 2 : 1;
   static constexpr int kDBlocks = D / 64;      // 64-column blocks of a row
   static constexpr int kKBlock = kTile * 128;  // 128 rows x 128 B
   static constexpr int kQBlock = kQ64 * 128;   // 64 rows x 128 B
-  alignas(1024) uint8_t k[kDBlocks * kKBlock];     // [D block][128 keys][64 d]
-  alignas(1024) uint8_t v[kDBlocks * kKBlock];
+  alignas(1024) uint8_t k[kKVBufs][kDBlocks * kKBlock];  // [buffer][D block][128 keys][64 d]
+  alignas(1024) uint8_t v[kKVBufs][kDBlocks * kKBlock];
   alignas(1024) uint8_t q[kQStages][kDBlocks * kQBlock];  // [stage][D block][64 queries][64 d]
   alignas(1024) uint8_t dO[kQStages][kDBlocks * kQBlock];
   alignas(1024) uint8_t dst[3][kKBlock];       // [tile % 3][128 keys][64 queries]
@@ -166,22 +168,26 @@ struct DkdvPipeSmem {
   // D = 64, atomic mode: drained dQ tiles [64 queries][D] for the bulk
   // reductions, double-buffered
   alignas(1024) float dq_stage[D == 64 ? 2 : 1][D == 64 ? kQ64 * D : 1];
-  uint64_t kv_full, qdo_full[kQStages], qdo_empty[kQStages], s_full[kBufs], s_read[kBufs], p_full[kBufs];
+  uint64_t kv_full[kKVBufs], kv_empty[kKVBufs];
+  uint64_t qdo_full[kQStages], qdo_empty[kQStages], s_full[kBufs], s_read[kBufs], p_full[kBufs];
   uint64_t buf_ready[kBufs];
-  uint64_t dq_full[3], tmem_free[kBufs], ds_last, all_done, drain[2];
+  uint64_t dq_full[3], tmem_free[kBufs], ds_last, acc_full, epi_read, drain[2];
   uint64_t stage_full[2], stage_free[2];
   uint32_t tmem_base;
   int abort_flag;
   uint32_t q_tiles[kSparse ? 2 * kMaxSparseTiles / 32 : 1];  // block-sparse: 64-row query tiles
 };
 
-template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse>
+template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse, bool kResident>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     bwd_dkdv_pipe_kernel(const __grid_constant__ BwdLaunch p) {
-  using Smem = DkdvPipeSmem<D, kSparse>;
+  static_assert(!kResident || (D == 64 && !kSparse),
+                "resident CTAs: D = 64 (two K / V buffers fit) and dense bands");
+  using Smem = DkdvPipeSmem<D, kSparse, kResident>;
   constexpr int kDB = Smem::kDBlocks;
-  constexpr int kNB = Smem::kBufs;  // S^T / dP^T buffers: tile it uses buffer it % kNB
-  constexpr int kQS = Smem::kQStages;  // Q / dO stages: tile it uses stage it % kQS
+  constexpr int kNB = Smem::kBufs;     // S^T / dP^T buffers: tile gi uses buffer gi % kNB
+  constexpr int kQS = Smem::kQStages;  // Q / dO stages: tile gi uses stage gi % kQS
+  constexpr int kKVB = Smem::kKVBufs;  // K / V buffers: unit k uses buffer k % kKVB
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -189,26 +195,61 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   const int n_kt = (p.N + kTile - 1) / kTile;
   const int Npad = n_kt * kTile;
   const int n_q64 = (p.N + kQ64 - 1) / kQ64;
-  // Head-major order, longest key tiles first within a head: the CTAs in
-  // flight share one head's Q, dO and dQ accumulator in L2.
-  // (tile-major instead when the streamed operands all fit in L2)
-  const int bh = static_cast<int>(p.tile_major ? blockIdx.x % p.BH : blockIdx.x / n_kt);
-  const int hh = bh % p.H, bb = bh / p.H;  // TMA coordinates of (batch, head)
-  const int kt = static_cast<int>(p.tile_major ? blockIdx.x / p.BH : blockIdx.x % n_kt);
-  const int k0 = kt * kTile;
+  const long long n_units = static_cast<long long>(n_kt) * p.BH;
   const int wl = p.band.win_left, wr = p.band.win_right;
-  int it_begin, it_last;  // 64-row query tiles whose band reaches this key tile
-  band_query_tiles(k0, kTile, kQ64, n_q64, wl, wr, it_begin, it_last);
-  const TileWalk<kSparse> walk{it_begin, it_last, n_q64, TileSet{s.q_tiles, n_q64}};
-  if constexpr (kSparse)  // the mask's 128-row blocks hold 64-row tiles 2b, 2b + 1
+  // A unit is one key tile of one (batch, head).  Head-major order, longest
+  // key tiles first within a head: the CTAs in flight share one head's Q, dO
+  // and dQ accumulator in L2 (tile-major instead when the streamed operands
+  // all fit in L2).  A CTA of the grid takes unit blockIdx.x; a resident
+  // CTA c of G takes units k G + c (k even) and k G + G - 1 - c (k odd).
+  auto unit_of = [&](int k) -> long long {
+    if constexpr (!kResident) return blockIdx.x;
+    const long long G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+  };
+  auto has_unit = [&](int k) { return kResident ? unit_of(k) < n_units : k == 0; };
+  struct Unit {
+    int bh, hh, bb, k0;  // slice, its TMA coordinates (head, batch), first key
+    int first, last;     // 64-row query tiles whose band reaches the key tile
+  };
+  auto decode = [&](long long u) {
+    Unit w;
+    w.bh = static_cast<int>(p.tile_major ? u % p.BH : u / n_kt);
+    w.hh = w.bh % p.H;
+    w.bb = w.bh / p.H;
+    w.k0 = static_cast<int>(p.tile_major ? u / p.BH : u % n_kt) * kTile;
+    band_query_tiles(w.k0, kTile, kQ64, n_q64, wl, wr, w.first, w.last);
+    return w;
+  };
+  auto walk_of = [&](const Unit& w) {
+    return TileWalk<kSparse>{w.first, w.last, n_q64, TileSet{s.q_tiles, n_q64}};
+  };
+  // fn(k, unit, walk) for this CTA's units in turn, while it returns true.
+  // Each role numbers the tiles of all its units in one sequence (gi) and
+  // every ring and buffer below is indexed by it.  A dense band reaches
+  // every key tile from at least one query tile (the tile holding the
+  // tile's first key), so a resident CTA's units are never empty.
+  auto for_each_unit = [&](auto&& fn) {
+    for (int k = 0; has_unit(k); ++k) {
+      const Unit w = decode(unit_of(k));
+      if (!fn(k, w, walk_of(w))) return false;
+    }
+    return true;
+  };
+  if constexpr (kSparse) {  // the mask's 128-row blocks hold 64-row tiles 2b, 2b + 1
+    const Unit w = decode(blockIdx.x);
     fill_tile_set(s.q_tiles, n_q64, [&](int it) {
-      return it >= it_begin && it <= it_last && block_kept(p.band, bh, p.H, n_kt, it >> 1, kt);
+      return it >= w.first && it <= w.last &&
+             block_kept(p.band, w.bh, p.H, n_kt, it >> 1, w.k0 / kTile);
     });
+  }
   __syncthreads();
-  const int n_it = walk.count();
 
   if (tid == 0) {
-    mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < kKVB; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
     for (int i = 0; i < kQS; ++i) {
       mbar_init(&s.qdo_full[i], 1);
       mbar_init(&s.qdo_empty[i], 1);
@@ -218,7 +259,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 256);
       mbar_init(&s.s_read[i], 8);  // one arrival per elementwise warp
-      // four buffer warps and the tcgen05.commit that retires dV, dK(it - kNB)
+      // four buffer warps and the tcgen05.commit that retires dV, dK(gi - kNB)
       mbar_init(&s.buf_ready[i], 5);
       mbar_init(&s.tmem_free[i], 128);
     }
@@ -228,7 +269,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       mbar_init(&s.stage_free[i], 1);  // the thread that issues the reductions
     }
     mbar_init(&s.ds_last, 256);
-    mbar_init(&s.all_done, 1);
+    mbar_init(&s.acc_full, 1);
+    mbar_init(&s.epi_read, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -247,30 +289,46 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&s.kv_full, 2 * kDB * Smem::kKBlock);
-      for (int kb = 0; kb < kDB; ++kb) {
-        tma_load_4d(s.k + kb * Smem::kKBlock, &p.map_k, &s.kv_full, kb * 64, k0, hh, bb);
-        tma_load_4d(s.v + kb * Smem::kKBlock, &p.map_v, &s.kv_full, kb * 64, k0, hh, bb);
-      }
-      int issued = 0;
-      for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-        const int st = it % kQS;
-        if (it >= kQS && !mbar_wait(&s.qdo_empty[st], ((it - kQS) / kQS) & 1, p.err, abort_flag))
-          break;
-        const int q0 = qt * kQ64;
-        mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
+      int kv_loads = 0, issued = 0;  // units whose K / V, tiles whose Q / dO were requested
+      int gi = 0;
+      for_each_unit([&](int k, const Unit& w, const TileWalk<kSparse>& walk) -> bool {
+        const int kvb = k % kKVB;
+        // buffer kvb was last read by the products of unit k - kKVB
+        if (k >= kKVB && !mbar_wait(&s.kv_empty[kvb], ((k - kKVB) / kKVB) & 1, p.err, abort_flag))
+          return false;
+        mbar_arrive_expect_tx(&s.kv_full[kvb], 2 * kDB * Smem::kKBlock);
         for (int kb = 0; kb < kDB; ++kb) {
-          tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0, hh, bb);
-          tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0, hh, bb);
+          tma_load_4d(s.k[kvb] + kb * Smem::kKBlock, &p.map_k, &s.kv_full[kvb], kb * 64, w.k0,
+                      w.hh, w.bb);
+          tma_load_4d(s.v[kvb] + kb * Smem::kKBlock, &p.map_v, &s.kv_full[kvb], kb * 64, w.k0,
+                      w.hh, w.bb);
         }
-        const long long off = static_cast<long long>(bh) * Npad + q0;
-        bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
-        bulk_load(s.di[st], p.di + off, kQ64 * 4, &s.qdo_full[st]);
-        issued = it + 1;
-      }
+        kv_loads = k + 1;
+        const int n = walk.count();
+        for (int i = 0, qt = walk.first(); i < n; ++i, qt = walk.next(qt), ++gi) {
+          const int st = gi % kQS;
+          if (gi >= kQS &&
+              !mbar_wait(&s.qdo_empty[st], ((gi - kQS) / kQS) & 1, p.err, abort_flag))
+            return false;
+          const int q0 = qt * kQ64;
+          mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
+          for (int kb = 0; kb < kDB; ++kb) {
+            tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0,
+                        w.hh, w.bb);
+            tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0,
+                        w.hh, w.bb);
+          }
+          const long long off = static_cast<long long>(w.bh) * Npad + q0;
+          bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
+          bulk_load(s.di[st], p.di + off, kQ64 * 4, &s.qdo_full[st]);
+          issued = gi + 1;
+        }
+        return true;
+      });
       if (*abort_flag) {
         int zero = 0;
-        mbar_wait(&s.kv_full, 0, p.err, &zero, 100000000ull);
+        for (int t = max(0, kv_loads - kKVB); t < kv_loads; ++t)
+          mbar_wait(&s.kv_full[t % kKVB], (t / kKVB) & 1, p.err, &zero, 100000000ull);
         for (int t = max(0, issued - kQS); t < issued; ++t)
           mbar_wait(&s.qdo_full[t % kQS], (t / kQS) & 1, p.err, &zero, 100000000ull);
       }
@@ -283,31 +341,39 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         if (leader) tc_commit(bar);
       };
       constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      bool ok = mbar_wait(&s.kv_full, 0, p.err, abort_flag);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int b = it % kNB, st = it % kQS;
-        // Buffer b may take tile it once buf_ready(it) completes: one wait
-        // here instead of three (each wait of this thread costs tensor time).
-        if (!mbar_wait(&s.buf_ready[b], (it / kNB) & 1, p.err, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+      int gi = 0;
+      for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
+        const int kvb = k % kKVB;
+        if (!mbar_wait(&s.kv_full[kvb], (k / kKVB) & 1, p.err, abort_flag)) return false;
+        const uint32_t k_addr = smem_u32(s.k[kvb]), v_addr = smem_u32(s.v[kvb]);
+        const int n = walk.count();
+        for (int i = 0; i < n; ++i, ++gi) {
+          const int b = gi % kNB, st = gi % kQS;
+          // Buffer b may take tile gi once buf_ready(gi) completes: one wait
+          // here instead of three (each wait of this thread costs tensor time).
+          if (!mbar_wait(&s.buf_ready[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-          const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-          if (leader) tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
-                    desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+            if (leader)
+              tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
+                        desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-          const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-          if (leader) tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
-                    desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+            if (leader)
+              tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
+                        desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+          }
+          leader_commit(&s.s_full[b]);
         }
-        leader_commit(&s.s_full[b]);
-      }
+        return true;
+      });
       leader_commit(&s.drain[0]);
       int zero = 0;
       mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
@@ -322,93 +388,113 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
       // d x queries, over keys; M = 128 at D = 64 too (rows past D unused)
       constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
-      const uint32_t k_addr = smem_u32(s.k);
-      bool ok = true;
-      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) % kNB.
-      auto issue_dq = [&](int j) {
+      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) % kNB,
+      // with K from buffer kvb.
+      auto issue_dq = [&](int j, int kvb) {
+        const uint32_t k_addr = smem_u32(s.k[kvb]);
         const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          if (leader) tc_mma_ss(tbase + ((j + 1) % kNB) * 128,
-                    desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
-                    desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128), idQ,
-                    kk > 0 ? 1u : 0u);
+          if (leader)
+            tc_mma_ss(tbase + ((j + 1) % kNB) * 128,
+                      desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
+                      desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128),
+                      idQ, kk > 0 ? 1u : 0u);
         leader_commit(&s.dq_full[j % 3]);
       };
-      for (int it = 0; it < n_it; ++it) {
-        const int b = it % kNB, st = it % kQS;
-        if (kAtomicDq && it >= 1) {
-          // S^T(it) is in the elementwise warps' registers: dQ^T(it - 1) can
-          // take its columns (their previous occupant, dQ^T(it - 1 - kNB), was
-          // drained before S^T(it) was issued), and dS^T(it - 1) reached
-          // shared memory before that signal.  It runs while the
-          // elementwise step of tile it does, off the chain that frees
-          // buffer b for S^T(it + 2).
-          if (!mbar_wait(&s.s_read[b], (it / kNB) & 1, p.err, abort_flag)) {
-            ok = false;
-            break;
+      int gi = 0;
+      int kvb_prev = 0;        // K / V buffer of tile gi - 1
+      bool prev_last = false;  // tile gi - 1 was the last of its unit
+      const bool ok = for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
+        const int kvb = k % kKVB;
+        const int n = walk.count();
+        for (int i = 0; i < n; ++i, ++gi) {
+          const int b = gi % kNB, st = gi % kQS;
+          if (kAtomicDq && gi >= 1) {
+            // S^T(gi) is in the elementwise warps' registers: dQ^T(gi - 1) can
+            // take its columns (their previous occupant, dQ^T(gi - 1 - kNB), was
+            // drained before S^T(gi) was issued), and dS^T(gi - 1) reached
+            // shared memory before that signal.  It runs while the
+            // elementwise step of tile gi does, off the chain that frees
+            // buffer b for S^T(gi + 2).
+            if (!mbar_wait(&s.s_read[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
+            tc_fence_after();
+            issue_dq(gi - 1, kvb_prev);
+            // the last product on the previous unit's K: its buffer is free
+            // for unit k + 1 once this completes
+            if (kResident && prev_last) leader_commit(&s.kv_empty[kvb_prev]);
           }
+          if (!mbar_wait(&s.p_full[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
           tc_fence_after();
-          issue_dq(it - 1);
-        }
-        if (!mbar_wait(&s.p_full[b], (it / kNB) & 1, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-        // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns
+          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+          // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns.  The
+          // first tile of a unit overwrites: the epilogue of the previous
+          // unit read dV, dK before its threads signalled p_full(gi).
 #pragma unroll
-        for (int kk = 0; kk < kQ64 / 16; ++kk)
-          if (leader) tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                    desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
+          for (int kk = 0; kk < kQ64 / 16; ++kk)
+            if (leader)
+              tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                        desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128),
+                        idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
 #pragma unroll
-        for (int kk = 0; kk < kQ64 / 16; ++kk)
-          if (leader) tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
-                    desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128), idKV,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        leader_commit(&s.qdo_empty[st]);
-        // dV, dK(it) done frees buffer b for tile it + kNB: the commit
-        // arrives on buf_ready(it + kNB) itself, so the score warp wakes on
-        // the tensor core's arrival, not on a relay.
-        leader_commit(&s.buf_ready[b]);
-      }
-      // The last tile's dQ^T goes into buffer n_it % kNB, once
-      // dQ^T(n_it - 1 - kNB) has left it and the last dS^T is in shared memory.
-      if (ok && kAtomicDq && !*abort_flag && n_it > 0) {
-        const int j = n_it - 1;
+          for (int kk = 0; kk < kQ64 / 16; ++kk)
+            if (leader)
+              tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                        desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128),
+                        idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          leader_commit(&s.qdo_empty[st]);
+          // dV, dK(gi) done frees buffer b for tile gi + kNB: the commit
+          // arrives on buf_ready(gi + kNB) itself, so the score warp wakes on
+          // the tensor core's arrival, not on a relay.
+          leader_commit(&s.buf_ready[b]);
+          kvb_prev = kvb;
+          prev_last = i == n - 1;
+        }
+        // dV, dK of this unit are complete once this arrives: the epilogue
+        // may read them.  The score products on this unit's K and V all
+        // completed before its last P^T / dS^T existed.
+        leader_commit(&s.acc_full);
+        if (kResident && !kAtomicDq) leader_commit(&s.kv_empty[kvb]);
+        return true;
+      });
+      // The CTA's last tile's dQ^T goes into buffer gi % kNB, once
+      // dQ^T(gi - 1 - kNB) has left it and the last dS^T is in shared memory.
+      if (ok && kAtomicDq && !*abort_flag && gi > 0) {
+        const int j = gi - 1;
         if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
             (j < kNB || mbar_wait(&s.tmem_free[(j + 1) % kNB], ((j - kNB) / kNB) & 1, p.err,
                                   abort_flag))) {
           tc_fence_after();
-          issue_dq(j);
+          issue_dq(j, kvb_prev);
         }
       }
-      // The score products all completed before the last P^T / dS^T existed,
-      // so this commit covers every product of the CTA.
-      leader_commit(&s.all_done);
       leader_commit(&s.drain[1]);
       int zero = 0;
       mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ buffer warps
-    // Buffer it % kNB may take S^T, dP^T(it) once dV, dK(it - kNB) are done
+    // Buffer gi % kNB may take S^T, dP^T(gi) once dV, dK(gi - kNB) are done
     // (the last readers of its P^T / dS^T; their tcgen05.commit arrives on
-    // buf_ready(it) directly), dQ^T(it - 1 - kNB) has left its S^T columns (atomic
-    // mode) and Q / dO(it) have landed.  These warps see to the last two,
-    // arrive on buf_ready(it), and in atomic mode drain dQ^T (TMEM lane =
-    // column d of dQ) into the fp32 accumulator.
+    // buf_ready(gi) directly), dQ^T(gi - 1 - kNB) has left its S^T columns
+    // (atomic mode) and Q / dO(gi) have landed.  These warps see to the last
+    // two, arrive on buf_ready(gi), and in atomic mode drain dQ^T (TMEM lane
+    // = column d of dQ) into the fp32 accumulator.
     const int quad = warp & 3;
     const int d = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    int qt_dq = walk.first();  // query tile of the dQ^T drained next
-    for (int it = 0; it < n_it + (kAtomicDq ? kNB + 1 : 0); ++it) {
-      const int b = it % kNB;
-      const int j = it - 1 - kNB;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) % kNB = b
-      const bool drain = kAtomicDq && j >= 0 && j < n_it;
+    int n_tiles = 0;  // tiles of all this CTA's units
+    for (int k = 0; has_unit(k); ++k) n_tiles += walk_of(decode(unit_of(k))).count();
+    // The drains run kNB + 1 tiles behind, into the next unit: the tile
+    // drained next is query tile qt_d of unit wd, with left_d tiles of it
+    // (this one included) still to drain.
+    int kd = 0, qt_d = 0, left_d = 0;
+    Unit wd{};
+    for (int gi = 0; gi < n_tiles + (kAtomicDq ? kNB + 1 : 0); ++gi) {
+      const int b = gi % kNB;
+      const int j = gi - 1 - kNB;  // dQ^T(j) sits in the S^T columns of buffer (j + 1) % kNB = b
+      const bool drain = kAtomicDq && j >= 0 && j < n_tiles;
       uint32_t g[2][32];
       if (drain) {
         if (!warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag)) break;
@@ -419,21 +505,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         tc_fence_before();
         mbar_arrive(&s.tmem_free[b]);  // for the last tile's dQ^T
       }
-      if (it < n_it) {
-        if (!warp_wait(&s.qdo_full[it % kQS], (it / kQS) & 1, p.err, abort_flag)) break;
+      if (gi < n_tiles) {
+        if (!warp_wait(&s.qdo_full[gi % kQS], (gi / kQS) & 1, p.err, abort_flag)) break;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&s.buf_ready[b]);
-          // the first kNB tiles have no dV, dK(it - kNB) to wait for
-          if (it < kNB && warp == 8) mbar_arrive(&s.buf_ready[b]);
+          // the first kNB tiles have no dV, dK(gi - kNB) to wait for
+          if (gi < kNB && warp == 8) mbar_arrive(&s.buf_ready[b]);
         }
       }
       if (drain) {
-        const int q0 = qt_dq * kQ64;
-        qt_dq = walk.next(qt_dq);
+        while (left_d == 0 && has_unit(kd)) {
+          wd = decode(unit_of(kd++));
+          left_d = walk_of(wd).count();
+          qt_d = walk_of(wd).first();
+        }
+        const int q0 = qt_d * kQ64;
+        --left_d;
+        qt_d = walk_of(wd).next(qt_d);
         if constexpr (D == 64) {
           // Stage the tile in shared memory ([query][d], rows d < 64 come
-          // from quadrants 0 and 1) and add it into the accumulator with one
+          // from quadrants 0 and 1) and add gi into the accumulator with one
           // bulk tensor reduction instead of 64 atomics per thread; rows
           // past N fall outside the tensor map and are dropped.
           const int sb = j & 1;
@@ -456,9 +548,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (lane == 0) {
               issued = mbar_wait(&s.stage_full[sb], (j >> 1) & 1, p.err, abort_flag);
               if (issued) {
-                tma_reduce_add_4d(&p.map_dqacc, s.dq_stage[sb], 0, q0, hh, bb);
+                tma_reduce_add_4d(&p.map_dqacc, s.dq_stage[sb], 0, q0, wd.hh, wd.bb);
                 tma_store_commit();
-                // the reduction of tile j - 1 has read its buffer: free it
+                // the reduction of tile j - 1 has read its buffer: free gi
                 tma_store_wait_read_all_but_newest();
                 if (j >= 1) mbar_arrive(&s.stage_free[(j - 1) & 1]);
               }
@@ -466,7 +558,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (!__all_sync(0xffffffffu, issued)) break;
           }
         } else {
-          float* dst = p.dq_accum + (static_cast<long long>(bh) * p.N + q0) * D + d;
+          float* dst = p.dq_accum + (static_cast<long long>(wd.bh) * p.N + q0) * D + d;
           const int nq = d < D ? min(kQ64, p.N - q0) : 0;  // lanes past D hold no dQ
 #pragma unroll
           for (int h = 0; h < 2; ++h)
@@ -477,7 +569,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
       }
     }
-    // the last bulk reductions must have read shared memory before it goes
+    // the last bulk reductions must have read shared memory before gi goes
     if (kAtomicDq && D == 64 && warp == 10 && lane == 0) tma_store_wait_all();
   } else {
     // ------------------------------------------------------------ elementwise
@@ -485,128 +577,147 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const int r = quad * 32 + lane;                // key row (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    const float nslope2 = kAlibi ? alibi_nslope2(p.band, bh, p.H) : 0.f;
-    bool ok = true;
-    for (int it = 0, qt = walk.first(); it < n_it; ++it, qt = walk.next(qt)) {
-      const int b = it % kNB, st = it % kQS;  // buffer, Q / dO stage
-      const int sd = it % 3;                   // dS^T stage
-      const int q0 = qt * kQ64;
-      // S^T(it) was issued after dV, dK(it - kNB), the last readers of the
-      // P^T / dS^T columns of buffer b, had completed.
-      if (!warp_wait(&s.s_full[b], (it / kNB) & 1, p.err, abort_flag) ||
-          !warp_wait(&s.qdo_full[st], (it / kQS) & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
-      tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
-      tmem_ld_wait();
-      if (kAtomicDq) {
-        // S^T(it) has left TMEM (and dS^T(it - 1), stored in the previous
-        // iteration, is in shared memory): dQ^T(it - 1) may overwrite it.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.s_read[b]);
-      }
-      const bool cut = band_cuts(q0, kQ64, k0, kTile, wl, wr);
-      // ALiBi on a tile wholly on one side of the diagonal: |key - q| is
-      // linear in the column, the bias B + D e (e = column of this half)
-      const bool below = k0 + kTile - 1 <= q0, above = q0 + kQ64 - 1 <= k0;
-      const bool lin = kAlibi && (below || above);
-      uint32_t pk[16], dk[16];
-      if (!cut && (!kAlibi || lin)) {
-        // P = 2^(S * scale * log2 e - LSE2 [+ bias]) and dS = P (dP - Di),
-        // two columns per packed instruction: the elementwise warps share
-        // their SM sub-partitions with the MMA-issuing warps, so every
-        // instruction saved here is issue time given back to the tensor core.
-        const uint64_t nsl2 = f32x2(-sl2, -sl2), neg1 = f32x2(-1.f, -1.f);
-        const float qk = static_cast<float>(q0 + half * 32 - (k0 + r));  // query - key at e = 0
-        const float sd = below ? nslope2 : -nslope2;
-        const uint64_t nb2 = f32x2(-sd * qk, -sd * qk), nd2 = f32x2(-sd, -sd);
-#pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = t + 2 * h;
-            uint64_t l2 = h ? f32x2(l4.z, l4.w) : f32x2(l4.x, l4.y);
-            if (lin)  // LSE2 - bias
-              l2 = fma_f32x2(f32x2(static_cast<float>(e), static_cast<float>(e + 1)), nd2,
-                             add_f32x2(l2, nb2));
-            // -z = LSE2 [- bias] - S * scale_log2
-            const float2 nz = split_f32x2(
-                fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, l2));
-            const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
-            const uint64_t dd =
-                fma_f32x2(h ? f32x2(d4.z, d4.w) : f32x2(d4.x, d4.y), neg1,
-                          f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])));
-            const float2 ds = split_f32x2(mul_f32x2(f32x2(p0, p1), dd));
-            pk[e / 2] = pack2<kBf16>(p0, p1);
-            dk[e / 2] = pack2<kBf16>(ds.x, ds.y);
-          }
-        }
-      } else {
-        // a tile the band cuts, or an ALiBi bias: key k0 + r, query q
-        const int key = k0 + r;
-#pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
-          const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q = q0 + half * 32 + t + e;
-            float z = fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]);
-            if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - q)), z);
-            float pe = ex2_approx(z);
-            if (cut && !band_visible(q, key, wl, wr)) pe = 0.f;
-            pv[e] = pe;
-            dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
-          }
-          pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
-          pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
-          dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
-          dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
-        }
-      }
-      // P^T and dS^T over this warp's own 32 dP^T columns (already read):
-      // P^T in the first 16, dS^T in the next 16.
-      tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
-      tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32 + 16, dk);
-      tmem_st_wait();
-      tc_fence_before();
-      // P(it) also publishes dS^T(it - 1), stored and fenced below in the
-      // previous iteration; dV, dK(it) need only the TMEM operands.
-      mbar_arrive(&s.p_full[b]);
-      if (kAtomicDq) {
-        // dQ^T(it - 3) was the last reader of dS^T buffer it % 3
-        if (it >= 3 && !warp_wait(&s.dq_full[sd], ((it - 3) / 3) & 1, p.err, abort_flag)) {
+    int gi = 0;
+    int epi_last = -3;  // resident: the last tile before the latest epilogue
+    for_each_unit([&](int k, const Unit& w, const TileWalk<kSparse>& walk) -> bool {
+      const int k0 = w.k0;
+      const float nslope2 = kAlibi ? alibi_nslope2(p.band, w.bh, p.H) : 0.f;
+      const int n = walk.count();
+      bool ok = true;
+      for (int i = 0, qt = walk.first(); i < n; ++i, qt = walk.next(qt), ++gi) {
+        const int b = gi % kNB, st = gi % kQS;  // buffer, Q / dO stage
+        const int sd = gi % 3;                   // dS^T stage
+        const int q0 = qt * kQ64;
+        // S^T(gi) was issued after dV, dK(gi - kNB), the last readers of the
+        // P^T / dS^T columns of buffer b, had completed.
+        if (!warp_wait(&s.s_full[b], (gi / kNB) & 1, p.err, abort_flag) ||
+            !warp_wait(&s.qdo_full[st], (gi / kQS) & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        store_row_chunk_sw128(s.dst[sd], r, half, dk);
-        fence_proxy_async_smem();
+        tc_fence_after();
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tbase + lane_off + b * 128 + half * 32, sr);
+        tmem_ld32(tbase + lane_off + b * 128 + 64 + half * 32, dr);
+        tmem_ld_wait();
+        if (kAtomicDq) {
+          // S^T(gi) has left TMEM (and dS^T(gi - 1), stored in the previous
+          // iteration, is in shared memory): dQ^T(gi - 1) may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.s_read[b]);
+        }
+        const bool cut = band_cuts(q0, kQ64, k0, kTile, wl, wr);
+        // ALiBi on a tile wholly on one side of the diagonal: |key - q| is
+        // linear in the column, the bias B + D e (e = column of this half)
+        const bool below = k0 + kTile - 1 <= q0, above = q0 + kQ64 - 1 <= k0;
+        const bool lin = kAlibi && (below || above);
+        uint32_t pk[16], dk[16];
+        if (!cut && (!kAlibi || lin)) {
+          // P = 2^(S * scale * log2 e - LSE2 [+ bias]) and dS = P (dP - Di),
+          // two columns per packed instruction: the elementwise warps share
+          // their SM sub-partitions with the MMA-issuing warps, so every
+          // instruction saved here is issue time given back to the tensor core.
+          const uint64_t nsl2 = f32x2(-sl2, -sl2), neg1 = f32x2(-1.f, -1.f);
+          const float qk = static_cast<float>(q0 + half * 32 - (k0 + r));  // query - key at e = 0
+          const float slope = below ? nslope2 : -nslope2;
+          const uint64_t nb2 = f32x2(-slope * qk, -slope * qk), nd2 = f32x2(-slope, -slope);
+#pragma unroll
+          for (int t = 0; t < 32; t += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = t + 2 * h;
+              uint64_t l2 = h ? f32x2(l4.z, l4.w) : f32x2(l4.x, l4.y);
+              if (lin)  // LSE2 - bias
+                l2 = fma_f32x2(f32x2(static_cast<float>(e), static_cast<float>(e + 1)), nd2,
+                               add_f32x2(l2, nb2));
+              // -z = LSE2 [- bias] - S * scale_log2
+              const float2 nz = split_f32x2(
+                  fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), nsl2, l2));
+              const float p0 = ex2_approx(-nz.x), p1 = ex2_approx(-nz.y);
+              const uint64_t dd =
+                  fma_f32x2(h ? f32x2(d4.z, d4.w) : f32x2(d4.x, d4.y), neg1,
+                            f32x2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])));
+              const float2 ds = split_f32x2(mul_f32x2(f32x2(p0, p1), dd));
+              pk[e / 2] = pack2<kBf16>(p0, p1);
+              dk[e / 2] = pack2<kBf16>(ds.x, ds.y);
+            }
+          }
+        } else {
+          // a tile the band cuts, or an ALiBi bias: key k0 + r, query q
+          const int key = k0 + r;
+#pragma unroll
+          for (int t = 0; t < 32; t += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&s.lse2[st][half * 32 + t]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&s.di[st][half * 32 + t]);
+            const float ll[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = q0 + half * 32 + t + e;
+              float z = fmaf(__uint_as_float(sr[t + e]), sl2, -ll[e]);
+              if (kAlibi) z = fmaf(nslope2, fabsf(static_cast<float>(key - q)), z);
+              float pe = ex2_approx(z);
+              if (cut && !band_visible(q, key, wl, wr)) pe = 0.f;
+              pv[e] = pe;
+              dsv[e] = pe * (__uint_as_float(dr[t + e]) - dd[e]);
+            }
+            pk[t / 2] = pack2<kBf16>(pv[0], pv[1]);
+            pk[t / 2 + 1] = pack2<kBf16>(pv[2], pv[3]);
+            dk[t / 2] = pack2<kBf16>(dsv[0], dsv[1]);
+            dk[t / 2 + 1] = pack2<kBf16>(dsv[2], dsv[3]);
+          }
+        }
+        // P^T and dS^T over this warp's own 32 dP^T columns (already read):
+        // P^T in the first 16, dS^T in the next 16.
+        tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32, pk);
+        tmem_st16(tbase + lane_off + b * 128 + 64 + half * 32 + 16, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        // P(gi) also publishes dS^T(gi - 1), stored and fenced below in the
+        // previous iteration; dV, dK(gi) need only the TMEM operands.
+        mbar_arrive(&s.p_full[b]);
+        if (kAtomicDq) {
+          // dQ^T(gi - 3) was the last reader of dS^T buffer gi % 3; resident,
+          // the two tiles after an epilogue find its dK, dV tiles there until
+          // their bulk stores have read them.
+          if ((gi >= 3 && !warp_wait(&s.dq_full[sd], ((gi - 3) / 3) & 1, p.err, abort_flag)) ||
+              (kResident && gi - epi_last <= 2 &&
+               !warp_wait(&s.epi_read, (k - 1) & 1, p.err, abort_flag))) {
+            ok = false;
+            break;
+          }
+          store_row_chunk_sw128(s.dst[sd], r, half, dk);
+          fence_proxy_async_smem();
+        }
       }
-    }
-    if (kAtomicDq && ok) mbar_arrive(&s.ds_last);
+      if (kAtomicDq && ok && !has_unit(k + 1)) mbar_arrive(&s.ds_last);
 
-    // ---------------------------------------------------------- epilogue
-    const bool done = ok && warp_wait(&s.all_done, 0, p.err, abort_flag);
-    if (named_bar_and(1, 256, done)) {
+      // -------------------------------------------------------- epilogue
+      // dK, dV staged in shared memory: the free Q / dO ring (16 or 32 KB
+      // of 32 or 48 each) of a CTA with one unit; a resident CTA's ring
+      // already holds its next unit's tiles, so it takes the dS^T buffers
+      // of tiles gl - 2 and gl - 1 (gl: this unit's last tile, gi - 1) once
+      // their dQ^T products and the previous epilogue's stores have read them.
+      const int gl = gi - 1;
+      uint8_t* dk_tile = kResident ? s.dst[(gl + 1) % 3] : s.q[0];
+      uint8_t* dv_tile = kResident ? s.dst[(gl + 2) % 3] : s.dO[0];
+      bool done = ok && warp_wait(&s.acc_full, k & 1, p.err, abort_flag);
+      if (kResident && done && k > 0) done = warp_wait(&s.epi_read, (k - 1) & 1, p.err, abort_flag);
+      if (kResident && kAtomicDq) {
+        for (int j = max(0, gl - 2); done && j < gl; ++j)
+          done = warp_wait(&s.dq_full[j % 3], (j / 3) & 1, p.err, abort_flag);
+      }
+      if (!named_bar_and(1, 256, done)) return false;
       tc_fence_after();
-      // D x 128 keys x 2 B of the free query ring each (16 or 32 KB of 32 or 48)
-      uint8_t* dk_tile = s.q[0];
-      uint8_t* dv_tile = s.dO[0];
 #pragma unroll 1
       for (int c = 0; c < kDB; ++c) {  // this warp's D / 2 columns, 32 at a time
         const int c32 = half * kDB + c;
         uint32_t a[32], g[32];
-        if (n_it > 0) {
+        if (n > 0) {
           tmem_ld32(tdV + lane_off + c32 * 32, a);
           tmem_ld32(tdK + lane_off + c32 * 32, g);
           tmem_ld_wait();
@@ -628,13 +739,21 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
       named_bar_sync(1, 256);
       if (tid == 0) {
         for (int kb = 0; kb < kDB; ++kb) {
-          tma_store_4d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
-          tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, hh, bb);
+          tma_store_4d(&p.map_dv, dv_tile + kb * Smem::kKBlock, kb * 64, k0, w.hh, w.bb);
+          tma_store_4d(&p.map_dk, dk_tile + kb * Smem::kKBlock, kb * 64, k0, w.hh, w.bb);
         }
         tma_store_commit();
-        tma_store_wait_all();
+        if constexpr (kResident) {
+          tma_store_wait_read_all();
+          mbar_arrive(&s.epi_read);
+        } else {
+          tma_store_wait_all();
+        }
       }
-    }
+      epi_last = gl;
+      return true;
+    });
+    if (kResident && tid == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -1046,19 +1165,37 @@ cudaError_t launch_dq_t(const BwdLaunch& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
-cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
-  auto kern = bwd_dkdv_pipe_kernel<D, kBf16, kAlibi, kAtomic, kSparse>;
-  const int smem = static_cast<int>(sizeof(DkdvPipeSmem<D, kSparse>)) + 1024;
+template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse, bool kResident>
+cudaError_t launch_dkdv_grid(const BwdLaunch& b, long long grid, cudaStream_t st) {
+  auto kern = bwd_dkdv_pipe_kernel<D, kBf16, kAlibi, kAtomic, kSparse, kResident>;
+  const int smem = static_cast<int>(sizeof(DkdvPipeSmem<D, kSparse, kResident>)) + 1024;
   static AttrCache configured;
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>((a.N + kTile - 1) / kTile) * a.BH;
-  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  BwdLaunch b = a;  // streamed per head: Q, dO and, atomic mode, the fp32 dQ accumulator
-  b.tile_major = tile_major_order(a.band, (kAtomic ? 8LL : 4LL) * a.BH * a.N * a.D);
   kern<<<static_cast<unsigned>(grid), kPipeThreads, smem, st>>>(b);
   return cudaGetLastError();
+}
+
+template <int D, bool kBf16, bool kAlibi, bool kAtomic, bool kSparse>
+cudaError_t launch_dkdv_pipe_t(const BwdLaunch& a, cudaStream_t st) {
+  const long long n_kt = (a.N + kTile - 1) / kTile;
+  const long long units = n_kt * a.BH;
+  if (units > INT_MAX) return cudaErrorInvalidConfiguration;
+  BwdLaunch b = a;  // streamed per head: Q, dO and, atomic mode, the fp32 dQ accumulator
+  b.tile_major = tile_major_order(a.band, (kAtomic ? 8LL : 4LL) * a.BH * a.N * a.D);
+  if constexpr (D == 64 && !kSparse) {
+    // Short sequences (at most 32 key tiles) with more key tiles than SMs:
+    // resident CTAs, one per SM, each loading its next key tile while it
+    // works on this one (a CTA per key tile spends about a third of its
+    // time starting, loading K, V and storing dK, dV at these lengths).
+    if (n_kt <= 32) {
+      int sms = 0;
+      const cudaError_t e = sm_count(&sms);
+      if (e != cudaSuccess) return e;
+      if (units > sms) return launch_dkdv_grid<D, kBf16, kAlibi, kAtomic, kSparse, true>(b, sms, st);
+    }
+  }
+  return launch_dkdv_grid<D, kBf16, kAlibi, kAtomic, kSparse, false>(b, units, st);
 }
 
 template <int D, bool kBf16, bool kSparse>

@@ -206,6 +206,11 @@ __device__ __forceinline__ void tma_store_wait_read_all_but_newest() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Wait until every committed bulk group has read its shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

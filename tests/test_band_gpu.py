@@ -80,6 +80,22 @@ def test_window_matches_oracle(B, H, N, D, dtype, causal, window):
     run_and_check(B, H, N, D, dtype, causal, window)
 
 
+RESIDENT = [
+    # More (batch, head, key tile) units than SMs at D = 64 and short N: the
+    # dK / dV kernel runs resident CTAs that take several units each, with
+    # ragged last key tiles and, under the identity window, one-tile units.
+    # (B, H, N, D, dtype, causal, (left, right), ALiBi)
+    (4, 40, 300, 64, "bf16", False, (32, 16), False),
+    (4, 40, 300, 64, "bf16", False, (0, 0), False),
+    (2, 80, 200, 64, "fp16", True, (-1, -1), True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,dtype,causal,window,use_alibi", RESIDENT)
+def test_resident_units_match_oracle(B, H, N, D, dtype, causal, window, use_alibi):
+    run_and_check(B, H, N, D, dtype, causal, window, alibi(B, H, True) if use_alibi else None)
+
+
 ALIBI = [
     # (B, H, N, D, dtype, causal, window, per_batch)
     (2, 3, 257, 64, "bf16", False, (-1, -1), False),

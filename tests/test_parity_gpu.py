@@ -151,6 +151,31 @@ def test_atomic_and_deterministic_backward_agree():
     assert float((a[0].float() - ref).abs().max()) <= 1e-2 * float(ref.abs().max())
 
 
+def test_resident_dkdv_is_bitwise_the_one_cta_per_tile_launch():
+    """With more key tiles than SMs at D = 64 the dK / dV kernel runs
+    resident CTAs, each taking several (batch, head, key tile) units in turn;
+    a unit's arithmetic does not depend on which CTA runs it, so one slice run
+    alone (eight units, one CTA each) gives bitwise the same dK and dV, and
+    the deterministic dQ as well."""
+    B, H, N, D = 2, 80, 1024, 64
+    w = W.custom(B, H, N, D, causal=True, seed=7)
+    g = U.gpu_inputs(w, W.make_inputs(w))
+    o, lse = U.run_forward(w, g)
+    w1 = W.custom(1, 1, N, D, causal=True, seed=7)  # the same sizes and scale for one slice
+    for det in (False, True):
+        dq, dk, dv = U.run_backward(w, g, o, lse, det)
+        for b, h in ((0, 0), (1, 37), (1, 79)):
+            def one(t):
+                return t[b:b + 1, h:h + 1].contiguous()
+            g1 = {k: one(v) for k, v in g.items()}
+            dq1, dk1, dv1 = U.run_backward(w1, g1, one(o), one(lse), det)
+            torch.cuda.synchronize()
+            assert torch.equal(dk1, one(dk)) and torch.equal(dv1, one(dv)), (det, b, h)
+            if det:
+                assert torch.equal(dq1, one(dq)), (b, h)
+    U.assert_no_device_error()
+
+
 def test_stage_entry_points_compose_to_fa_bwd():
     w = W.custom(2, 2, 384, 128, causal=True, seed=5)
     g = U.gpu_inputs(w, W.make_inputs(w))
