@@ -8,7 +8,8 @@
 // as well as (batch, head), the sequence-dimension split of FlashAttention-2
 // ("FlashAttention 深入", v2).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads; warps 10 and 11 only lend their registers to
+// the softmax warps, see kFwdThreads):
 //   warps 0-3  softmax for tile A, warps 4-7 softmax for tile B: thread t of
 //              a group owns query row t of its tile (= TMEM lane t).  Reads S
 //              from TMEM, keeps the running max m and sum l in fp32
@@ -71,7 +72,14 @@
 namespace fa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+// 12 warps: 0-7 softmax, 8 producer, 9 MMA, 10-11 idle.  The launch
+// reserves 168 registers a thread (three warps share each SM sub-partition's
+// 16384); warpgroup 2 (warps 8-11) gives up all but kFwdLowRegs and the two
+// softmax warpgroups take kFwdHighRegs: 256 x 208 + 128 x 80 = 63488 of the
+// 384 x 168 = 64512 reserved, and 32 x (208 + 208 + 80) = 15872 registers on
+// each sub-partition.
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kFwdLowRegs = 80, kFwdHighRegs = 208;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D, bool kSparse, bool kFp8>
@@ -288,267 +296,273 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.map_q);
-      tma_prefetch_desc(&p.map_k);
-      tma_prefetch_desc(&p.map_v);
-      uint32_t kv = 0;      // K/V tiles loaded so far, over all units (ring position)
-      int q_rounds = 0;     // Q loads issued
-      long long loads = 0;  // K and V loads issued (K of ring position n is load 2n)
-      for_each_unit([&](int k, long long u) -> bool {
-        FwdUnit w;
-        decode(u, w);
-        const KeyWalk<kSparse> walk = walk_of(w);
-        // The running counters are copied in and out, so that the key-tile
-        // loop works on registers.
-        uint32_t ring = kv;
-        long long n_loads = loads;
-        // Unit k's Q goes into set k % kQSets once the last S product of the
-        // unit that used the set before has read it.
-        const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;
-        if (q_use > 0 && !mbar_wait(&s.q_empty[qs], (q_use - 1) & 1, p.err, abort_flag))
-          return false;
-        mbar_arrive_expect_tx(&s.q_full[qs], w.n_q_here * Smem::kTileBytes);
-        for (int t = 0; t < w.n_q_here; ++t)
-          for (int kb = 0; kb < Smem::kBlocks; ++kb)
-            tma_load_4d(s.q[qs][t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full[qs],
-                        kb * kColsPerBlock, (2 * w.pt + t) * kTile, w.hh, w.bb);
-        q_rounds = k + 1;
-        bool stop = false;
-        for (int j = walk.first(); j < walk.n; j = walk.next(j), ++ring) {
-          const int st = ring & 1;
-          const uint32_t use = ring >> 1;  // earlier uses of this stage
-          if (ring >= 2 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, p.err, abort_flag)) {
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
-          for (int kb = 0; kb < Smem::kBlocks; ++kb)
-            tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st],
-                        kb * kColsPerBlock, j * kTile, w.hh, w.bb);
-          ++n_loads;
-          if (ring >= 2 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, p.err, abort_flag)) {
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
-          if constexpr (kFp8) {
-            // V^T rows d = 0..D-1, keys j*128 .. j*128+127
-            tma_load_4d(s.v[st], &p.map_v, &s.v_full[st], j * kTile, 0, w.hh, w.bb);
-          } else {
+  if (warp >= 8) {
+    // The producer and MMA warps need few registers: their warpgroup
+    // gives some to the softmax warpgroups (warps 10 and 11 only do this).
+    setmaxnreg_dec<kFwdLowRegs>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&p.map_q);
+        tma_prefetch_desc(&p.map_k);
+        tma_prefetch_desc(&p.map_v);
+        uint32_t kv = 0;      // K/V tiles loaded so far, over all units (ring position)
+        int q_rounds = 0;     // Q loads issued
+        long long loads = 0;  // K and V loads issued (K of ring position n is load 2n)
+        for_each_unit([&](int k, long long u) -> bool {
+          FwdUnit w;
+          decode(u, w);
+          const KeyWalk<kSparse> walk = walk_of(w);
+          // The running counters are copied in and out, so that the key-tile
+          // loop works on registers.
+          uint32_t ring = kv;
+          long long n_loads = loads;
+          // Unit k's Q goes into set k % kQSets once the last S product of the
+          // unit that used the set before has read it.
+          const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;
+          if (q_use > 0 && !mbar_wait(&s.q_empty[qs], (q_use - 1) & 1, p.err, abort_flag))
+            return false;
+          mbar_arrive_expect_tx(&s.q_full[qs], w.n_q_here * Smem::kTileBytes);
+          for (int t = 0; t < w.n_q_here; ++t)
             for (int kb = 0; kb < Smem::kBlocks; ++kb)
-              tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
-                          j * kTile, w.hh, w.bb);
+              tma_load_4d(s.q[qs][t] + kb * Smem::kBlockBytes, &p.map_q, &s.q_full[qs],
+                          kb * kColsPerBlock, (2 * w.pt + t) * kTile, w.hh, w.bb);
+          q_rounds = k + 1;
+          bool stop = false;
+          for (int j = walk.first(); j < walk.n; j = walk.next(j), ++ring) {
+            const int st = ring & 1;
+            const uint32_t use = ring >> 1;  // earlier uses of this stage
+            if (ring >= 2 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, p.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&s.k_full[st], Smem::kTileBytes);
+            for (int kb = 0; kb < Smem::kBlocks; ++kb)
+              tma_load_4d(s.k[st] + kb * Smem::kBlockBytes, &p.map_k, &s.k_full[st],
+                          kb * kColsPerBlock, j * kTile, w.hh, w.bb);
+            ++n_loads;
+            if (ring >= 2 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, p.err, abort_flag)) {
+              stop = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&s.v_full[st], Smem::kTileBytes);
+            if constexpr (kFp8) {
+              // V^T rows d = 0..D-1, keys j*128 .. j*128+127
+              tma_load_4d(s.v[st], &p.map_v, &s.v_full[st], j * kTile, 0, w.hh, w.bb);
+            } else {
+              for (int kb = 0; kb < Smem::kBlocks; ++kb)
+                tma_load_4d(s.v[st] + kb * Smem::kBlockBytes, &p.map_v, &s.v_full[st], kb * 64,
+                            j * kTile, w.hh, w.bb);
+            }
+            ++n_loads;
           }
-          ++n_loads;
-        }
-        kv = ring;
-        loads = n_loads;
-        return !stop;
-      });
-      if (*abort_flag) {
-        // Let copies already in flight land before the CTA's smem goes away.
-        int zero = 0;
-        for (int r = max(0, q_rounds - Smem::kQSets); r < q_rounds; ++r)
-          mbar_wait(&s.q_full[r % Smem::kQSets], (r / Smem::kQSets) & 1, p.err, &zero,
-                    100000000ull);
-        for (long long t = loads > 4 ? loads - 4 : 0; t < loads; ++t) {
-          const long long n = t >> 1;  // ring position
-          const int st = static_cast<int>(n & 1);
-          mbar_wait((t & 1) ? &s.v_full[st] : &s.k_full[st], static_cast<uint32_t>((n >> 1) & 1),
-                    p.err, &zero, 100000000ull);
+          kv = ring;
+          loads = n_loads;
+          return !stop;
+        });
+        if (*abort_flag) {
+          // Let copies already in flight land before the CTA's smem goes away.
+          int zero = 0;
+          for (int r = max(0, q_rounds - Smem::kQSets); r < q_rounds; ++r)
+            mbar_wait(&s.q_full[r % Smem::kQSets], (r / Smem::kQSets) & 1, p.err, &zero,
+                      100000000ull);
+          for (long long t = loads > 4 ? loads - 4 : 0; t < loads; ++t) {
+            const long long n = t >> 1;  // ring position
+            const int st = static_cast<int>(n & 1);
+            mbar_wait((t & 1) ? &s.v_full[st] : &s.k_full[st], static_cast<uint32_t>((n >> 1) & 1),
+                      p.err, &zero, 100000000ull);
+          }
         }
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // 16-bit operands: every lane computes the same descriptors and waits
-    // on the same barriers; only the elected lane issues.  (A single-lane
-    // branch made each product's operands per-thread values to be moved into
-    // uniform registers first: issuing a group's sixteen products then took
-    // longer than the tensor core took to run them.)  8-bit operands keep
-    // the single-lane loop.
-    if (!kFp8 || lane == 0) {
-      const bool leader = kFp8 ? true : elect_one_sync();
-      auto leader_commit = [&](uint64_t* bar) {
-        if (leader) tc_commit(bar);
-      };
-      constexpr uint32_t ab = kBf16 ? 1u : 0u;
-      constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, ab, 0, 0);
-      // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
-      constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, D) : idesc_f16(128, D, ab, 0, 1);
-      // Operand descriptors are built once and advanced by constant offsets.
-      const uint64_t dq0 = kRows64 ? smem_desc_sw64(smem_u32(s.q[0][0]), 16, 512)
-                                   : smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
-      const uint64_t dk0 = kRows64 ? smem_desc_sw64(smem_u32(s.k[0]), 16, 512)
-                                   : smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
-      const uint64_t dv0 =
-          smem_desc_sw128(smem_u32(s.v[0]), kFp8 ? 16 : Smem::kBlockBytes, 1024);
-      // One product step covers 32 bytes of each row: 16 elements of 16 bits,
-      // 32 of 8 bits.
-      constexpr int kStepElems = kFp8 ? 32 : 16;
-      // P step kk of V tile stage st: 16-bit V advances kStepElems rows of
-      // 128 bytes, 8-bit V^T 32 bytes within each row.
-      auto v_step = [](uint64_t dv, int kk) {
-        return kFp8 ? desc_add(dv, kk * 32) : desc_add(dv, kk * kStepElems * 128);
-      };
-      uint32_t kv_run = 0;              // K/V tiles of earlier units (ring position)
-      int base0_run = 0, base1_run = 0;  // P V products of tiles A, B in earlier units
-      for_each_unit([&](int k, long long u) -> bool {
-        FwdUnit w;
-        decode(u, w);
-        const KeyWalk<kSparse> walk = walk_of(w);
-        const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;  // this unit's Q set
-        // register copies of the running counters for this unit's loops
-        const uint32_t kv = kv_run;
-        const int base0 = base0_run, base1 = base1_run;
-        // S products of this unit still to issue; with resident CTAs the
-        // last one's commit hands the Q buffers to the next unit's loads.
-        [[maybe_unused]] int s_left = walk.count_of(0) + walk.count_of(1);
-        // S_t = Q_t K^T into tile t's S columns, K from stage kst
-        auto issue_s = [&](int t, int kst) {
-          const uint64_t dq = desc_add(dq0, (qs * 2 + t) * Smem::kTileBytes);
-          const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
-            const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
-            if (leader) mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
-                         kk > 0 ? 1u : 0u);
-          }
-          leader_commit(&s.s_full[t]);
-          if constexpr (kResident)
-            if (--s_left == 0) leader_commit(&s.q_empty[qs]);
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      // 16-bit operands: every lane computes the same descriptors and waits
+      // on the same barriers; only the elected lane issues.  (A single-lane
+      // branch made each product's operands per-thread values to be moved into
+      // uniform registers first: issuing a group's sixteen products then took
+      // longer than the tensor core took to run them.)  8-bit operands keep
+      // the single-lane loop.
+      if (!kFp8 || lane == 0) {
+        const bool leader = kFp8 ? true : elect_one_sync();
+        auto leader_commit = [&](uint64_t* bar) {
+          if (leader) tc_commit(bar);
         };
-        const int jf = walk.first();
-        // with nothing to multiply (an empty block-sparse pair) no K arrives
-        bool ok = mbar_wait_poll(&s.q_full[qs], q_use & 1, p.err, abort_flag) &&
-                  (jf >= walk.n || mbar_wait_poll(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
-        if (!ok) return false;
-        if (jf >= walk.n) {
-          if constexpr (kResident) leader_commit(&s.q_empty[qs]);
-          return true;
-        }
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (walk.has(t, jf)) issue_s(t, kv & 1);
-        leader_commit(&s.k_empty[kv & 1]);
-        int n_stream = 0;  // key tiles in this unit's K/V stream
-        if constexpr (!kSparse) {
-          // dense: each tile's key tiles are the range [lo_t, hi_t]
-          const int j_first = jf, j_last = walk.last;
-          for (int j = j_first; ok && j <= j_last; ++j) {
-            const uint32_t g = kv + static_cast<uint32_t>(j - j_first);  // ring position of j
-            const int st = g & 1;
-            if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
-              ok = false;
-              break;
+        constexpr uint32_t ab = kBf16 ? 1u : 0u;
+        constexpr uint32_t idS = kFp8 ? idesc_e4m3(128, 128) : idesc_f16(128, 128, ab, 0, 0);
+        // P V: 16-bit V is MN-major (D contiguous); 8-bit V^T is K-major
+        constexpr uint32_t idPV = kFp8 ? idesc_e4m3(128, D) : idesc_f16(128, D, ab, 0, 1);
+        // Operand descriptors are built once and advanced by constant offsets.
+        const uint64_t dq0 = kRows64 ? smem_desc_sw64(smem_u32(s.q[0][0]), 16, 512)
+                                     : smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
+        const uint64_t dk0 = kRows64 ? smem_desc_sw64(smem_u32(s.k[0]), 16, 512)
+                                     : smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+        const uint64_t dv0 =
+            smem_desc_sw128(smem_u32(s.v[0]), kFp8 ? 16 : Smem::kBlockBytes, 1024);
+        // One product step covers 32 bytes of each row: 16 elements of 16 bits,
+        // 32 of 8 bits.
+        constexpr int kStepElems = kFp8 ? 32 : 16;
+        // P step kk of V tile stage st: 16-bit V advances kStepElems rows of
+        // 128 bytes, 8-bit V^T 32 bytes within each row.
+        auto v_step = [](uint64_t dv, int kk) {
+          return kFp8 ? desc_add(dv, kk * 32) : desc_add(dv, kk * kStepElems * 128);
+        };
+        uint32_t kv_run = 0;              // K/V tiles of earlier units (ring position)
+        int base0_run = 0, base1_run = 0;  // P V products of tiles A, B in earlier units
+        for_each_unit([&](int k, long long u) -> bool {
+          FwdUnit w;
+          decode(u, w);
+          const KeyWalk<kSparse> walk = walk_of(w);
+          const int qs = k % Smem::kQSets, q_use = k / Smem::kQSets;  // this unit's Q set
+          // register copies of the running counters for this unit's loops
+          const uint32_t kv = kv_run;
+          const int base0 = base0_run, base1 = base1_run;
+          // S products of this unit still to issue; with resident CTAs the
+          // last one's commit hands the Q buffers to the next unit's loads.
+          [[maybe_unused]] int s_left = walk.count_of(0) + walk.count_of(1);
+          // S_t = Q_t K^T into tile t's S columns, K from stage kst
+          auto issue_s = [&](int t, int kst) {
+            const uint64_t dq = desc_add(dq0, (qs * 2 + t) * Smem::kTileBytes);
+            const uint64_t dk = desc_add(dk0, kst * Smem::kTileBytes);
+  #pragma unroll
+            for (int kk = 0; kk < Smem::kRowBytes / 32; ++kk) {
+              const uint32_t off = (kk >> 2) * Smem::kBlockBytes + (kk & 3) * 32;
+              if (leader) mma_ss<kFp8>(tbase + t * 128, desc_add(dq, off), desc_add(dk, off), idS,
+                           kk > 0 ? 1u : 0u);
             }
-            bool k_next = false;  // K_{j+1} has landed
-            for (int t = 0; ok && t < 2; ++t) {
-              // (selects, not indexing: a dynamic index would put w in local memory)
-              const int lt = t ? w.lo[1] : w.lo[0], ht = t ? w.hi[1] : w.hi[0];
-              const bool active = j >= lt && j <= ht;
-              // S_t(j+1) is next: after PV_t(j), or as the first product of
-              // a tile whose range starts at j + 1
-              const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
-              if (active) {
-                if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + j - lt) & 1, p.err,
-                               abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                // O_t += P_t(j) V_j, with P read from tile t's S columns
-                const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                  if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
-                               idPV, (j > lt || kk > 0) ? 1u : 0u);
-                leader_commit(&s.o_done[t]);
+            leader_commit(&s.s_full[t]);
+            if constexpr (kResident)
+              if (--s_left == 0) leader_commit(&s.q_empty[qs]);
+          };
+          const int jf = walk.first();
+          // with nothing to multiply (an empty block-sparse pair) no K arrives
+          bool ok = mbar_wait_poll(&s.q_full[qs], q_use & 1, p.err, abort_flag) &&
+                    (jf >= walk.n || mbar_wait_poll(&s.k_full[kv & 1], (kv >> 1) & 1, p.err, abort_flag));
+          if (!ok) return false;
+          if (jf >= walk.n) {
+            if constexpr (kResident) leader_commit(&s.q_empty[qs]);
+            return true;
+          }
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (walk.has(t, jf)) issue_s(t, kv & 1);
+          leader_commit(&s.k_empty[kv & 1]);
+          int n_stream = 0;  // key tiles in this unit's K/V stream
+          if constexpr (!kSparse) {
+            // dense: each tile's key tiles are the range [lo_t, hi_t]
+            const int j_first = jf, j_last = walk.last;
+            for (int j = j_first; ok && j <= j_last; ++j) {
+              const uint32_t g = kv + static_cast<uint32_t>(j - j_first);  // ring position of j
+              const int st = g & 1;
+              if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+                ok = false;
+                break;
               }
-              if (s_next) {
-                if (!k_next) {
-                  if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+              bool k_next = false;  // K_{j+1} has landed
+              for (int t = 0; ok && t < 2; ++t) {
+                // (selects, not indexing: a dynamic index would put w in local memory)
+                const int lt = t ? w.lo[1] : w.lo[0], ht = t ? w.hi[1] : w.hi[0];
+                const bool active = j >= lt && j <= ht;
+                // S_t(j+1) is next: after PV_t(j), or as the first product of
+                // a tile whose range starts at j + 1
+                const bool s_next = active ? j + 1 <= ht : (j + 1 == lt && lt <= ht);
+                if (active) {
+                  if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + j - lt) & 1, p.err,
                                  abort_flag)) {
                     ok = false;
                     break;
                   }
                   tc_fence_after();
-                  k_next = true;
+                  // O_t += P_t(j) V_j, with P read from tile t's S columns
+                  const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+  #pragma unroll
+                  for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                    if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                                 idPV, (j > lt || kk > 0) ? 1u : 0u);
+                  leader_commit(&s.o_done[t]);
                 }
-                issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
-              }
-            }
-            leader_commit(&s.v_empty[st]);
-            if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
-          }
-          n_stream = j_last - j_first + 1;
-        } else {
-          // block-sparse: each tile's key tiles are a set; counters give the
-          // p_full phases
-          int c0 = 0, c1 = 0;  // P V products issued for tile A, B
-          for (int j = jf, jn = 0; ok && j < walk.n; j = jn, ++n_stream) {
-            jn = walk.next(j);  // the stream's next key tile
-            const uint32_t g = kv + static_cast<uint32_t>(n_stream);
-            const int st = g & 1;
-            if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
-              ok = false;
-              break;
-            }
-            bool k_next = false;  // K of tile jn has landed
-            for (int t = 0; ok && t < 2; ++t) {
-              const bool active = walk.has(t, j);
-              // S_t of tile jn follows PV_t(j), or starts a tile that joins at jn
-              const bool s_next = jn < walk.n && walk.has(t, jn);
-              if (active) {
-                const int ct = t ? c1 : c0;
-                if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + ct) & 1, p.err, abort_flag)) {
-                  ok = false;
-                  break;
+                if (s_next) {
+                  if (!k_next) {
+                    if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                                   abort_flag)) {
+                      ok = false;
+                      break;
+                    }
+                    tc_fence_after();
+                    k_next = true;
+                  }
+                  issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
                 }
-                tc_fence_after();
-                // O_t += P_t(j) V_j, with P read from tile t's S columns
-                const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTile / kStepElems; ++kk)
-                  if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
-                               idPV, (ct > 0 || kk > 0) ? 1u : 0u);
-                leader_commit(&s.o_done[t]);
-                if (t)
-                  ++c1;
-                else
-                  ++c0;
               }
-              if (s_next) {
-                if (!k_next) {
-                  if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
-                                 abort_flag)) {
+              leader_commit(&s.v_empty[st]);
+              if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
+            }
+            n_stream = j_last - j_first + 1;
+          } else {
+            // block-sparse: each tile's key tiles are a set; counters give the
+            // p_full phases
+            int c0 = 0, c1 = 0;  // P V products issued for tile A, B
+            for (int j = jf, jn = 0; ok && j < walk.n; j = jn, ++n_stream) {
+              jn = walk.next(j);  // the stream's next key tile
+              const uint32_t g = kv + static_cast<uint32_t>(n_stream);
+              const int st = g & 1;
+              if (!mbar_wait_poll(&s.v_full[st], (g >> 1) & 1, p.err, abort_flag)) {
+                ok = false;
+                break;
+              }
+              bool k_next = false;  // K of tile jn has landed
+              for (int t = 0; ok && t < 2; ++t) {
+                const bool active = walk.has(t, j);
+                // S_t of tile jn follows PV_t(j), or starts a tile that joins at jn
+                const bool s_next = jn < walk.n && walk.has(t, jn);
+                if (active) {
+                  const int ct = t ? c1 : c0;
+                  if (!mbar_wait_poll(&s.p_full[t], ((t ? base1 : base0) + ct) & 1, p.err, abort_flag)) {
                     ok = false;
                     break;
                   }
                   tc_fence_after();
-                  k_next = true;
+                  // O_t += P_t(j) V_j, with P read from tile t's S columns
+                  const uint64_t dv = desc_add(dv0, st * Smem::kTileBytes);
+  #pragma unroll
+                  for (int kk = 0; kk < kTile / kStepElems; ++kk)
+                    if (leader) mma_ts<kFp8>(tbase + 256 + t * D, tbase + t * 128 + kk * 8, v_step(dv, kk),
+                                 idPV, (ct > 0 || kk > 0) ? 1u : 0u);
+                  leader_commit(&s.o_done[t]);
+                  if (t)
+                    ++c1;
+                  else
+                    ++c0;
                 }
-                issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
+                if (s_next) {
+                  if (!k_next) {
+                    if (!mbar_wait_poll(&s.k_full[(g + 1) & 1], ((g + 1) >> 1) & 1, p.err,
+                                   abort_flag)) {
+                      ok = false;
+                      break;
+                    }
+                    tc_fence_after();
+                    k_next = true;
+                  }
+                  issue_s(t, (g + 1) & 1);  // after the PV product that read P_t(j)
+                }
               }
+              leader_commit(&s.v_empty[st]);
+              if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
             }
-            leader_commit(&s.v_empty[st]);
-            if (k_next) leader_commit(&s.k_empty[(g + 1) & 1]);
           }
-        }
-        kv_run = kv + static_cast<uint32_t>(n_stream);
-        base0_run = base0 + walk.count_of(0);
-        base1_run = base1 + walk.count_of(1);
-        return ok;
-      });
-      // Every MMA issued above completes before TMEM is released.
-      leader_commit(&s.drain);
-      int zero = 0;
-      mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+          kv_run = kv + static_cast<uint32_t>(n_stream);
+          base0_run = base0 + walk.count_of(0);
+          base1_run = base1 + walk.count_of(1);
+          return ok;
+        });
+        // Every MMA issued above completes before TMEM is released.
+        leader_commit(&s.drain);
+        int zero = 0;
+        mbar_wait(&s.drain, 0, p.err, &zero, 100000000ull);
+      }
     }
   } else {
+    setmaxnreg_inc<kFwdHighRegs>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;          // query tile of this group (0 = A, 1 = B)
     const int r = tid & 127;          // row within the tile and TMEM lane

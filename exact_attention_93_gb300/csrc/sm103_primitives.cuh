@@ -206,6 +206,17 @@ __device__ __forceinline__ void tma_store_wait_read_all_but_newest() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Per-warpgroup register budget (every warp of the warpgroup executes it):
+// give registers back to the block's pool, or take them from it.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // Wait until every committed bulk group has read its shared-memory source.
 __device__ __forceinline__ void tma_store_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
