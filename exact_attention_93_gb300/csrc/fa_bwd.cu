@@ -1258,8 +1258,11 @@ cudaError_t launch_bwd_dq(const BwdLaunch& a, cudaStream_t st) {
 cudaError_t launch_dq_convert(const float* acc, void* dq, RowStrides sdq, int N, int H,
                               long long BH, int D, float scale, int bf16, cudaStream_t st) {
   const long long n8 = BH * N * D / 8;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  int sms = 0;
+  const cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  long long blocks = (n8 + 255) / 256;  // grid-stride, at most 16 CTAs per SM
+  if (blocks > 16LL * sms) blocks = 16LL * sms;
   if (blocks < 1) blocks = 1;
   auto* d16 = static_cast<uint16_t*>(dq);
   const unsigned g = static_cast<unsigned>(blocks);
