@@ -75,6 +75,27 @@ cudaError_t ensure_dynamic_smem(K kern, int bytes, AttrCache& cache) {
 }
 
 // Streaming multiprocessors of the current device (cached per device).
+// Launches kern with programmatic stream serialization: its CTAs may start
+// while the preceding kernel in the stream runs its last ones, instead of
+// after it.  A kernel launched this way starts with pdl_wait_and_release()
+// (sm103_primitives.cuh), which returns once that kernel has completed and
+// its writes are visible, before it touches global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 inline cudaError_t sm_count(int* out) {
   static std::atomic<int> cached[64] = {};
   int dev = 0;

@@ -217,6 +217,15 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (at once when the launch
+// did not allow overlap), then let a following kernel launched the same way
+// start once every CTA of this grid has passed here.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Wait until every committed bulk group has read its shared-memory source.
 __device__ __forceinline__ void tma_store_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

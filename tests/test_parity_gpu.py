@@ -176,6 +176,26 @@ def test_resident_dkdv_is_bitwise_the_one_cta_per_tile_launch():
     U.assert_no_device_error()
 
 
+def test_forward_sees_inputs_written_just_before_it():
+    """The forward kernel may start while the preceding kernel in the stream
+    finishes (programmatic stream serialization); it must still read the
+    inputs that kernel writes.  Two forwards back to back on the GPT-2
+    shape, with q negated in place between them by a torch kernel, give bit
+    for bit the forward of a fresh negated copy."""
+    w = W.WORKLOADS["gpt2_causal"]
+    g = U.gpu_inputs(w, W.make_inputs(w, with_grad_output=False))
+    o1, l1 = U.run_forward(w, g)
+    g["q"].neg_()
+    o2, l2 = U.run_forward(w, g)
+    fresh = {k: v.clone() for k, v in g.items()}
+    torch.cuda.synchronize()
+    o3, l3 = U.run_forward(w, fresh)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o3) and torch.equal(l2, l3)
+    assert not torch.equal(o1, o2)
+    U.assert_no_device_error()
+
+
 def test_stage_entry_points_compose_to_fa_bwd():
     w = W.custom(2, 2, 384, 128, causal=True, seed=5)
     g = U.gpu_inputs(w, W.make_inputs(w))
