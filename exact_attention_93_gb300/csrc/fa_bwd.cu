@@ -142,7 +142,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 // At D = 64 the dQ^T product still runs with M = 128: output row m depends
 // only on A row m, so rows 64..127 (read past K's tile in shared memory) are
 // computed and never drained.
-constexpr int kPipeThreads = 480;  // warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA
+// Warps 0-7 elementwise, 8-11 buffer / dQ, 12 producer, 13-14 MMA (and at
+// D = 64 an idle warp 15).  At D = 64 the launch reserves 128 registers a
+// thread for 16 warps (four share each SM sub-partition's 16384); warpgroup
+// 3 (warps 12-15) keeps kPipeLowRegs and the elementwise warpgroups take
+// kPipeHighRegs: 256 x 144 + 128 x 128 + 128 x 88 = 64512 of the 65536
+// reserved, 32 x (144 + 144 + 128 + 88) = 16128 on each sub-partition.  (At
+// D = 128 the same split made the kernel slower.)
+template <int D>
+constexpr int kPipeThreads = D == 64 ? 512 : 480;
+constexpr uint32_t kPipeLowRegs = 88, kPipeHighRegs = 144;
 constexpr int kQ64 = 64;
 
 template <int D, bool kSparse, bool kResident>
@@ -179,7 +188,7 @@ struct DkdvPipeSmem {
 };
 
 template <int D, bool kBf16, bool kAlibi, bool kAtomicDq, bool kSparse, bool kResident>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+__global__ void __launch_bounds__(kPipeThreads<D>, 1)
     bwd_dkdv_pipe_kernel(const __grid_constant__ BwdLaunch p) {
   static_assert(!kResident || (D == 64 && !kSparse),
                 "resident CTAs: D = 64 (two K / V buffers fit) and dense bands");
@@ -286,192 +295,197 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   volatile int* abort_flag = &s.abort_flag;
   constexpr uint32_t ab = kBf16 ? 1u : 0u;
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int kv_loads = 0, issued = 0;  // units whose K / V, tiles whose Q / dO were requested
-      int gi = 0;
-      for_each_unit([&](int k, const Unit& w, const TileWalk<kSparse>& walk) -> bool {
-        const int kvb = k % kKVB;
-        // buffer kvb was last read by the products of unit k - kKVB
-        if (k >= kKVB && !mbar_wait(&s.kv_empty[kvb], ((k - kKVB) / kKVB) & 1, p.err, abort_flag))
-          return false;
-        mbar_arrive_expect_tx(&s.kv_full[kvb], 2 * kDB * Smem::kKBlock);
-        for (int kb = 0; kb < kDB; ++kb) {
-          tma_load_4d(s.k[kvb] + kb * Smem::kKBlock, &p.map_k, &s.kv_full[kvb], kb * 64, w.k0,
-                      w.hh, w.bb);
-          tma_load_4d(s.v[kvb] + kb * Smem::kKBlock, &p.map_v, &s.kv_full[kvb], kb * 64, w.k0,
-                      w.hh, w.bb);
-        }
-        kv_loads = k + 1;
-        const int n = walk.count();
-        for (int i = 0, qt = walk.first(); i < n; ++i, qt = walk.next(qt), ++gi) {
-          const int st = gi % kQS;
-          if (gi >= kQS &&
-              !mbar_wait(&s.qdo_empty[st], ((gi - kQS) / kQS) & 1, p.err, abort_flag))
+  if (warp >= 12) {
+    // D = 64: the producer and MMA warps give registers to the elementwise
+    // warpgroups (warp 15 only does this)
+    if constexpr (D == 64) setmaxnreg_dec<kPipeLowRegs>();
+    if (warp == 12) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int kv_loads = 0, issued = 0;  // units whose K / V, tiles whose Q / dO were requested
+        int gi = 0;
+        for_each_unit([&](int k, const Unit& w, const TileWalk<kSparse>& walk) -> bool {
+          const int kvb = k % kKVB;
+          // buffer kvb was last read by the products of unit k - kKVB
+          if (k >= kKVB && !mbar_wait(&s.kv_empty[kvb], ((k - kKVB) / kKVB) & 1, p.err, abort_flag))
             return false;
-          const int q0 = qt * kQ64;
-          mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
+          mbar_arrive_expect_tx(&s.kv_full[kvb], 2 * kDB * Smem::kKBlock);
           for (int kb = 0; kb < kDB; ++kb) {
-            tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0,
+            tma_load_4d(s.k[kvb] + kb * Smem::kKBlock, &p.map_k, &s.kv_full[kvb], kb * 64, w.k0,
                         w.hh, w.bb);
-            tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0,
+            tma_load_4d(s.v[kvb] + kb * Smem::kKBlock, &p.map_v, &s.kv_full[kvb], kb * 64, w.k0,
                         w.hh, w.bb);
           }
-          const long long off = static_cast<long long>(w.bh) * Npad + q0;
-          bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
-          bulk_load(s.di[st], p.di + off, kQ64 * 4, &s.qdo_full[st]);
-          issued = gi + 1;
+          kv_loads = k + 1;
+          const int n = walk.count();
+          for (int i = 0, qt = walk.first(); i < n; ++i, qt = walk.next(qt), ++gi) {
+            const int st = gi % kQS;
+            if (gi >= kQS &&
+                !mbar_wait(&s.qdo_empty[st], ((gi - kQS) / kQS) & 1, p.err, abort_flag))
+              return false;
+            const int q0 = qt * kQ64;
+            mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
+            for (int kb = 0; kb < kDB; ++kb) {
+              tma_load_4d(s.q[st] + kb * Smem::kQBlock, &p.map_q64, &s.qdo_full[st], kb * 64, q0,
+                          w.hh, w.bb);
+              tma_load_4d(s.dO[st] + kb * Smem::kQBlock, &p.map_do64, &s.qdo_full[st], kb * 64, q0,
+                          w.hh, w.bb);
+            }
+            const long long off = static_cast<long long>(w.bh) * Npad + q0;
+            bulk_load(s.lse2[st], p.lse + off, kQ64 * 4, &s.qdo_full[st]);
+            bulk_load(s.di[st], p.di + off, kQ64 * 4, &s.qdo_full[st]);
+            issued = gi + 1;
+          }
+          return true;
+        });
+        if (*abort_flag) {
+          int zero = 0;
+          for (int t = max(0, kv_loads - kKVB); t < kv_loads; ++t)
+            mbar_wait(&s.kv_full[t % kKVB], (t / kKVB) & 1, p.err, &zero, 100000000ull);
+          for (int t = max(0, issued - kQS); t < issued; ++t)
+            mbar_wait(&s.qdo_full[t % kQS], (t / kQS) & 1, p.err, &zero, 100000000ull);
         }
-        return true;
-      });
-      if (*abort_flag) {
-        int zero = 0;
-        for (int t = max(0, kv_loads - kKVB); t < kv_loads; ++t)
-          mbar_wait(&s.kv_full[t % kKVB], (t / kKVB) & 1, p.err, &zero, 100000000ull);
-        for (int t = max(0, issued - kQS); t < issued; ++t)
-          mbar_wait(&s.qdo_full[t % kQS], (t / kQS) & 1, p.err, &zero, 100000000ull);
       }
-    }
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ score products
-    {
-      const bool leader = elect_one_sync();
-      auto leader_commit = [&](uint64_t* bar) {
-        if (leader) tc_commit(bar);
-      };
-      constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
-      int gi = 0;
-      for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
-        const int kvb = k % kKVB;
-        if (!mbar_wait(&s.kv_full[kvb], (k / kKVB) & 1, p.err, abort_flag)) return false;
-        const uint32_t k_addr = smem_u32(s.k[kvb]), v_addr = smem_u32(s.v[kvb]);
-        const int n = walk.count();
-        for (int i = 0; i < n; ++i, ++gi) {
-          const int b = gi % kNB, st = gi % kQS;
-          // Buffer b may take tile gi once buf_ready(gi) completes: one wait
-          // here instead of three (each wait of this thread costs tensor time).
-          if (!mbar_wait(&s.buf_ready[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            if (leader)
-              tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
-                        desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
-            const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
-            if (leader)
-              tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
-                        desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
-          }
-          leader_commit(&s.s_full[b]);
-        }
-        return true;
-      });
-      leader_commit(&s.drain[0]);
-      int zero = 0;
-      mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
-    }
-  } else if (warp == 14) {
-    // ------------------------------------------------------------ gradient products
-    {
-      const bool leader = elect_one_sync();
-      auto leader_commit = [&](uint64_t* bar) {
-        if (leader) tc_commit(bar);
-      };
-      constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
-      // d x queries, over keys; M = 128 at D = 64 too (rows past D unused)
-      constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
-      // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) % kNB,
-      // with K from buffer kvb.
-      auto issue_dq = [&](int j, int kvb) {
-        const uint32_t k_addr = smem_u32(s.k[kvb]);
-        const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          if (leader)
-            tc_mma_ss(tbase + ((j + 1) % kNB) * 128,
-                      desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
-                      desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128),
-                      idQ, kk > 0 ? 1u : 0u);
-        leader_commit(&s.dq_full[j % 3]);
-      };
-      int gi = 0;
-      int kvb_prev = 0;        // K / V buffer of tile gi - 1
-      bool prev_last = false;  // tile gi - 1 was the last of its unit
-      const bool ok = for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
-        const int kvb = k % kKVB;
-        const int n = walk.count();
-        for (int i = 0; i < n; ++i, ++gi) {
-          const int b = gi % kNB, st = gi % kQS;
-          if (kAtomicDq && gi >= 1) {
-            // S^T(gi) is in the elementwise warps' registers: dQ^T(gi - 1) can
-            // take its columns (their previous occupant, dQ^T(gi - 1 - kNB), was
-            // drained before S^T(gi) was issued), and dS^T(gi - 1) reached
-            // shared memory before that signal.  It runs while the
-            // elementwise step of tile gi does, off the chain that frees
-            // buffer b for S^T(gi + 2).
-            if (!mbar_wait(&s.s_read[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
+    } else if (warp == 13) {
+      // ------------------------------------------------------------ score products
+      {
+        const bool leader = elect_one_sync();
+        auto leader_commit = [&](uint64_t* bar) {
+          if (leader) tc_commit(bar);
+        };
+        constexpr uint32_t idS = idesc_f16(128, kQ64, ab, 0, 0);  // keys x queries, over d
+        int gi = 0;
+        for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
+          const int kvb = k % kKVB;
+          if (!mbar_wait(&s.kv_full[kvb], (k / kKVB) & 1, p.err, abort_flag)) return false;
+          const uint32_t k_addr = smem_u32(s.k[kvb]), v_addr = smem_u32(s.v[kvb]);
+          const int n = walk.count();
+          for (int i = 0; i < n; ++i, ++gi) {
+            const int b = gi % kNB, st = gi % kQS;
+            // Buffer b may take tile gi once buf_ready(gi) completes: one wait
+            // here instead of three (each wait of this thread costs tensor time).
+            if (!mbar_wait(&s.buf_ready[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
             tc_fence_after();
-            issue_dq(gi - 1, kvb_prev);
-            // the last product on the previous unit's K: its buffer is free
-            // for unit k + 1 once this completes
-            if (kResident && prev_last) leader_commit(&s.kv_empty[kvb_prev]);
+            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+              const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+              if (leader)
+                tc_mma_ss(tbase + b * 128, desc_add(smem_desc_sw128(k_addr, 16, 1024), ka),
+                          desc_add(smem_desc_sw128(q_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ka = (kk >> 2) * Smem::kKBlock + (kk & 3) * 32;
+              const uint32_t kq = (kk >> 2) * Smem::kQBlock + (kk & 3) * 32;
+              if (leader)
+                tc_mma_ss(tbase + b * 128 + 64, desc_add(smem_desc_sw128(v_addr, 16, 1024), ka),
+                          desc_add(smem_desc_sw128(do_addr, 16, 1024), kq), idS, kk > 0 ? 1u : 0u);
+            }
+            leader_commit(&s.s_full[b]);
           }
-          if (!mbar_wait(&s.p_full[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
-          // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns.  The
-          // first tile of a unit overwrites: the epilogue of the previous
-          // unit read dV, dK before its threads signalled p_full(gi).
-#pragma unroll
-          for (int kk = 0; kk < kQ64 / 16; ++kk)
-            if (leader)
-              tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                        desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128),
-                        idKV, (i > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
-#pragma unroll
-          for (int kk = 0; kk < kQ64 / 16; ++kk)
-            if (leader)
-              tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
-                        desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128),
-                        idKV, (i > 0 || kk > 0) ? 1u : 0u);
-          leader_commit(&s.qdo_empty[st]);
-          // dV, dK(gi) done frees buffer b for tile gi + kNB: the commit
-          // arrives on buf_ready(gi + kNB) itself, so the score warp wakes on
-          // the tensor core's arrival, not on a relay.
-          leader_commit(&s.buf_ready[b]);
-          kvb_prev = kvb;
-          prev_last = i == n - 1;
-        }
-        // dV, dK of this unit are complete once this arrives: the epilogue
-        // may read them.  The score products on this unit's K and V all
-        // completed before its last P^T / dS^T existed.
-        leader_commit(&s.acc_full);
-        if (kResident && !kAtomicDq) leader_commit(&s.kv_empty[kvb]);
-        return true;
-      });
-      // The CTA's last tile's dQ^T goes into buffer gi % kNB, once
-      // dQ^T(gi - 1 - kNB) has left it and the last dS^T is in shared memory.
-      if (ok && kAtomicDq && !*abort_flag && gi > 0) {
-        const int j = gi - 1;
-        if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
-            (j < kNB || mbar_wait(&s.tmem_free[(j + 1) % kNB], ((j - kNB) / kNB) & 1, p.err,
-                                  abort_flag))) {
-          tc_fence_after();
-          issue_dq(j, kvb_prev);
-        }
+          return true;
+        });
+        leader_commit(&s.drain[0]);
+        int zero = 0;
+        mbar_wait(&s.drain[0], 0, p.err, &zero, 100000000ull);
       }
-      leader_commit(&s.drain[1]);
-      int zero = 0;
-      mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
+    } else if (warp == 14) {
+      // ------------------------------------------------------------ gradient products
+      {
+        const bool leader = elect_one_sync();
+        auto leader_commit = [&](uint64_t* bar) {
+          if (leader) tc_commit(bar);
+        };
+        constexpr uint32_t idKV = idesc_f16(128, D, ab, 0, 1);    // keys x d, over queries
+        // d x queries, over keys; M = 128 at D = 64 too (rows past D unused)
+        constexpr uint32_t idQ = idesc_f16(128, kQ64, ab, 1, 1);
+        // dQ^T(j) = K^T dS^T(j), into the S^T columns of buffer (j + 1) % kNB,
+        // with K from buffer kvb.
+        auto issue_dq = [&](int j, int kvb) {
+          const uint32_t k_addr = smem_u32(s.k[kvb]);
+          const uint32_t dst_addr = smem_u32(s.dst[j % 3]);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            if (leader)
+              tc_mma_ss(tbase + ((j + 1) % kNB) * 128,
+                        desc_add(smem_desc_sw128(k_addr, Smem::kKBlock, 1024), kk * 16 * 128),
+                        desc_add(smem_desc_sw128(dst_addr, Smem::kKBlock, 1024), kk * 16 * 128),
+                        idQ, kk > 0 ? 1u : 0u);
+          leader_commit(&s.dq_full[j % 3]);
+        };
+        int gi = 0;
+        int kvb_prev = 0;        // K / V buffer of tile gi - 1
+        bool prev_last = false;  // tile gi - 1 was the last of its unit
+        const bool ok = for_each_unit([&](int k, const Unit&, const TileWalk<kSparse>& walk) -> bool {
+          const int kvb = k % kKVB;
+          const int n = walk.count();
+          for (int i = 0; i < n; ++i, ++gi) {
+            const int b = gi % kNB, st = gi % kQS;
+            if (kAtomicDq && gi >= 1) {
+              // S^T(gi) is in the elementwise warps' registers: dQ^T(gi - 1) can
+              // take its columns (their previous occupant, dQ^T(gi - 1 - kNB), was
+              // drained before S^T(gi) was issued), and dS^T(gi - 1) reached
+              // shared memory before that signal.  It runs while the
+              // elementwise step of tile gi does, off the chain that frees
+              // buffer b for S^T(gi + 2).
+              if (!mbar_wait(&s.s_read[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
+              tc_fence_after();
+              issue_dq(gi - 1, kvb_prev);
+              // the last product on the previous unit's K: its buffer is free
+              // for unit k + 1 once this completes
+              if (kResident && prev_last) leader_commit(&s.kv_empty[kvb_prev]);
+            }
+            if (!mbar_wait(&s.p_full[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dO[st]);
+            // dV += P^T dO : A = P^T packed in TMEM over the dP^T columns.  The
+            // first tile of a unit overwrites: the epilogue of the previous
+            // unit read dV, dK before its threads signalled p_full(gi).
+#pragma unroll
+            for (int kk = 0; kk < kQ64 / 16; ++kk)
+              if (leader)
+                tc_mma_ts(tdV, tbase + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                          desc_add(smem_desc_sw128(do_addr, Smem::kQBlock, 1024), kk * 16 * 128),
+                          idKV, (i > 0 || kk > 0) ? 1u : 0u);
+            // dK += dS^T Q : A = dS^T packed in TMEM beside P^T
+#pragma unroll
+            for (int kk = 0; kk < kQ64 / 16; ++kk)
+              if (leader)
+                tc_mma_ts(tdK, tbase + b * 128 + 64 + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                          desc_add(smem_desc_sw128(q_addr, Smem::kQBlock, 1024), kk * 16 * 128),
+                          idKV, (i > 0 || kk > 0) ? 1u : 0u);
+            leader_commit(&s.qdo_empty[st]);
+            // dV, dK(gi) done frees buffer b for tile gi + kNB: the commit
+            // arrives on buf_ready(gi + kNB) itself, so the score warp wakes on
+            // the tensor core's arrival, not on a relay.
+            leader_commit(&s.buf_ready[b]);
+            kvb_prev = kvb;
+            prev_last = i == n - 1;
+          }
+          // dV, dK of this unit are complete once this arrives: the epilogue
+          // may read them.  The score products on this unit's K and V all
+          // completed before its last P^T / dS^T existed.
+          leader_commit(&s.acc_full);
+          if (kResident && !kAtomicDq) leader_commit(&s.kv_empty[kvb]);
+          return true;
+        });
+        // The CTA's last tile's dQ^T goes into buffer gi % kNB, once
+        // dQ^T(gi - 1 - kNB) has left it and the last dS^T is in shared memory.
+        if (ok && kAtomicDq && !*abort_flag && gi > 0) {
+          const int j = gi - 1;
+          if (mbar_wait(&s.ds_last, 0, p.err, abort_flag) &&
+              (j < kNB || mbar_wait(&s.tmem_free[(j + 1) % kNB], ((j - kNB) / kNB) & 1, p.err,
+                                    abort_flag))) {
+            tc_fence_after();
+            issue_dq(j, kvb_prev);
+          }
+        }
+        leader_commit(&s.drain[1]);
+        int zero = 0;
+        mbar_wait(&s.drain[1], 0, p.err, &zero, 100000000ull);
+      }
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ buffer warps
@@ -572,6 +586,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // the last bulk reductions must have read shared memory before gi goes
     if (kAtomicDq && D == 64 && warp == 10 && lane == 0) tma_store_wait_all();
   } else {
+    if constexpr (D == 64) setmaxnreg_inc<kPipeHighRegs>();
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, query-column half
     const int r = quad * 32 + lane;                // key row (TMEM lane)
@@ -1172,7 +1187,7 @@ cudaError_t launch_dkdv_grid(const BwdLaunch& b, long long grid, cudaStream_t st
   static AttrCache configured;
   cudaError_t e = ensure_dynamic_smem(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(grid), kPipeThreads, smem, st>>>(b);
+  kern<<<static_cast<unsigned>(grid), kPipeThreads<D>, smem, st>>>(b);
   return cudaGetLastError();
 }
 
