@@ -137,6 +137,13 @@ typedef struct {
  * above the diagonal are skipped.  `scale` must be finite (the usual value is
  * 1/sqrt(D), [API] softmax_scale default).  Writes o and lse only.
  * Deterministic: the same inputs give bit-identical outputs.
+ *
+ * The forward kernel (of every fa_fwd* call) is launched with programmatic
+ * stream serialization: its CTAs may start while the preceding kernel in
+ * the stream finishes, and wait for that kernel's completion before
+ * reading anything.  Stream order is kept for every caller; a following
+ * kernel that itself allows overlap must, as always, wait
+ * (cudaGridDependencySynchronize) before reading o or lse.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int D, float scale, int causal, fa_dtype dtype, void* stream);
