@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
         qt_d = walk_of(wd).next(qt_d);
         if constexpr (D == 64) {
           // Stage the tile in shared memory ([query][d], rows d < 64 come
-          // from quadrants 0 and 1) and add gi into the accumulator with one
+          // from quadrants 0 and 1) and add it into the accumulator with one
           // bulk tensor reduction instead of 64 atomics per thread; rows
           // past N fall outside the tensor map and are dropped.
           const int sb = j & 1;
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
               if (issued) {
                 tma_reduce_add_4d(&p.map_dqacc, s.dq_stage[sb], 0, q0, wd.hh, wd.bb);
                 tma_store_commit();
-                // the reduction of tile j - 1 has read its buffer: free gi
+                // the reduction of tile j - 1 has read its buffer: free it
                 tma_store_wait_read_all_but_newest();
                 if (j >= 1) mbar_arrive(&s.stage_free[(j - 1) & 1]);
               }
@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
         }
       }
     }
-    // the last bulk reductions must have read shared memory before gi goes
+    // the last bulk reductions must have read shared memory before it goes
     if (kAtomicDq && D == 64 && warp == 10 && lane == 0) tma_store_wait_all();
   } else {
     if constexpr (D == 64) setmaxnreg_inc<kPipeHighRegs>();
