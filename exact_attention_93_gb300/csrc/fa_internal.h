@@ -74,12 +74,12 @@ cudaError_t ensure_dynamic_smem(K kern, int bytes, AttrCache& cache) {
   return e;
 }
 
-// Streaming multiprocessors of the current device (cached per device).
 // Launches kern with programmatic stream serialization: its CTAs may start
 // while the preceding kernel in the stream runs its last ones, instead of
-// after it.  A kernel launched this way starts with pdl_wait_and_release()
-// (sm103_primitives.cuh), which returns once that kernel has completed and
-// its writes are visible, before it touches global memory.
+// after it.  A kernel launched this way starts with pdl_wait() or
+// pdl_wait_and_release() (sm103_primitives.cuh), which return once that
+// kernel has completed and its writes are visible, before it touches global
+// memory.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
                               cudaStream_t stream, Args&&... args) {
@@ -96,6 +96,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned bl
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Streaming multiprocessors of the current device (cached per device).
 inline cudaError_t sm_count(int* out) {
   static std::atomic<int> cached[64] = {};
   int dev = 0;

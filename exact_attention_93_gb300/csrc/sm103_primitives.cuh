@@ -221,6 +221,11 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 // stream has completed and its writes are visible (at once when the launch
 // did not allow overlap), then let a following kernel launched the same way
 // start once every CTA of this grid has passed here.
+// The waiting half alone: a kernel that never signals lets the next kernel
+// launched with overlap start as each of its CTAs exits, so no CTA waiting
+// here holds an SM that this grid's own later CTAs could use.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

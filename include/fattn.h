@@ -236,6 +236,10 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int D, int deterministic);
  *   no atomics; results are bit-identical across runs ([API] deterministic).
  * `workspace` must hold fa_bwd_workspace_size(...) bytes, 256-byte aligned;
  * its contents on entry do not matter.
+ *
+ * Its kernels are launched with programmatic stream serialization: each may
+ * start while the kernel before it in the stream finishes, and waits for
+ * that kernel's completion before reading anything (as fa_fwd's does).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int D,
