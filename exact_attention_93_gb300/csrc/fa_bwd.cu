@@ -182,6 +182,7 @@ struct DkdvPipeSmem {
   uint64_t qdo_full[kQStages], qdo_empty[kQStages], s_full[kBufs], s_read[kBufs], p_full[kBufs];
   uint64_t buf_ready[kBufs];
   uint64_t dq_full[3], tmem_free[kBufs], ds_last, acc_full, epi_read, drain[2];
+  uint64_t last_issued;  // resident: a unit's last dV, dK issued
   uint64_t stage_full[2], stage_free[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
     mbar_init(&s.ds_last, 256);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.epi_read, 1);
+    mbar_init(&s.last_issued, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -364,6 +366,12 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
           const int n = walk.count();
           for (int i = 0; i < n; ++i, ++gi) {
             const int b = gi % kNB, st = gi % kQS;
+            // A unit's products follow the previous unit's last dV, dK into
+            // the tensor core's queue: the epilogue waits for those, not for
+            // scores the elementwise warps need only after it.
+            if (kResident && i == 0 && k > 0 &&
+                !mbar_wait(&s.last_issued, (k - 1) & 1, p.err, abort_flag))
+              return false;
             // Buffer b may take tile gi once buf_ready(gi) completes: one wait
             // here instead of three (each wait of this thread costs tensor time).
             if (!mbar_wait(&s.buf_ready[b], (gi / kNB) & 1, p.err, abort_flag)) return false;
@@ -463,6 +471,10 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
             // arrives on buf_ready(gi + kNB) itself, so the score warp wakes on
             // the tensor core's arrival, not on a relay.
             leader_commit(&s.buf_ready[b]);
+            if (kResident && i == n - 1) {
+              __syncwarp();
+              if (leader) mbar_arrive(&s.last_issued);
+            }
             kvb_prev = kvb;
             prev_last = i == n - 1;
           }
@@ -596,6 +608,16 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
     const float sl2 = p.scale_log2;
     int gi = 0;
     int epi_last = -3;  // resident: the last tile before the latest epilogue
+    // resident, thread 0: the latest epilogue's store has still to be
+    // waited for and epi_read signalled (done before anyone waits on it)
+    bool epi_signal = false;
+    auto signal_epi_read = [&] {
+      if (kResident && tid == 0 && epi_signal) {
+        tma_store_wait_read_all();
+        mbar_arrive(&s.epi_read);
+        epi_signal = false;
+      }
+    };
     for_each_unit([&](int k, const Unit& w, const TileWalk<kSparse>& walk) -> bool {
       const int k0 = w.k0;
       const float nslope2 = kAlibi ? alibi_nslope2(p.band, w.bh, p.H) : 0.f;
@@ -701,6 +723,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
           // dQ^T(gi - 3) was the last reader of dS^T buffer gi % 3; resident,
           // the two tiles after an epilogue find its dK, dV tiles there until
           // their bulk stores have read them.
+          signal_epi_read();
           if ((gi >= 3 && !warp_wait(&s.dq_full[sd], ((gi - 3) / 3) & 1, p.err, abort_flag)) ||
               (kResident && gi - epi_last <= 2 &&
                !warp_wait(&s.epi_read, (k - 1) & 1, p.err, abort_flag))) {
@@ -723,6 +746,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
       uint8_t* dk_tile = kResident ? s.dst[(gl + 1) % 3] : s.q[0];
       uint8_t* dv_tile = kResident ? s.dst[(gl + 2) % 3] : s.dO[0];
       bool done = ok && warp_wait(&s.acc_full, k & 1, p.err, abort_flag);
+      signal_epi_read();
       if (kResident && done && k > 0) done = warp_wait(&s.epi_read, (k - 1) & 1, p.err, abort_flag);
       if (kResident && kAtomicDq) {
         for (int j = max(0, gl - 2); done && j < gl; ++j)
@@ -761,8 +785,7 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
         }
         tma_store_commit();
         if constexpr (kResident) {
-          tma_store_wait_read_all();
-          mbar_arrive(&s.epi_read);
+          epi_signal = true;
         } else {
           tma_store_wait_all();
         }

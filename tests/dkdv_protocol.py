@@ -49,8 +49,15 @@ class DkdvPipeline:
     buffers (3 at D = 64, 2 at D = 128); resident: several units per CTA
     (D = 64 only); atomic_dq: dQ^T products and their drain."""
 
-    def __init__(self, units, buffers, resident, atomic_dq, d64, seed, skip=frozenset()):
+    def __init__(self, units, buffers, resident, atomic_dq, d64, seed, skip=frozenset(),
+                 independent_signal=False):
         self.rng = random.Random(seed)
+        # independent_signal: epi_read signalled by its own role as soon as
+        # the store has read its staging, instead of by thread 0 just before
+        # the first wait on it (every arrival time the kernel can produce,
+        # and more: the elementwise role stands for all eight warps, so with
+        # the inline signal its own waits on epi_read are always satisfied)
+        self.independent_signal = independent_signal
         self.units, self.nb, self.res, self.atomic, self.d64 = list(units), buffers, resident, atomic_dq, d64
         self.nqs = buffers + 1               # Q / dO stages
         self.nkv = 2 if resident else 1      # K / V buffers
@@ -70,6 +77,7 @@ class DkdvPipeline:
         self.stage_full = [B(f"stage_full{i}", 2) for i in range(2)]
         self.stage_free = [B(f"stage_free{i}", 1) for i in range(2)]
         self.ds_last, self.acc_full, self.epi_read = B("ds_last", 1), B("acc_full", 1), B("epi_read", 1)
+        self.last_issued = B("last_issued", 1)  # resident: a unit's last dV, dK issued
         self.drain = [B("drain0", 1), B("drain1", 1)]
         self.q_score, self.q_grad = [], []  # tensor-core issue queues, each in order
         self.copies = []                    # asynchronous copies in flight (any order)
@@ -140,8 +148,10 @@ class DkdvPipeline:
         for k, n in enumerate(self.units):
             kvb = k % self.nkv
             yield from self.wait(self.kv_full[kvb], k // self.nkv, "score.kv_full")
-            for _ in range(n):
+            for i in range(n):
                 b, st = gi % self.nb, gi % self.nqs
+                if self.res and i == 0 and k > 0:
+                    yield from self.wait(self.last_issued, k - 1, "score.last_issued")
                 yield from self.wait(self.buf_ready[b], gi // self.nb, "score.buf_ready")
 
                 def products(b=b, st=st, gi=gi, kvb=kvb, k=k):
@@ -214,6 +224,8 @@ class DkdvPipeline:
                 self.q_grad.append(("mma", products))
                 self.q_grad.append(("commit", self.qdo_empty[st]))
                 self.q_grad.append(("commit", self.buf_ready[b]))
+                if self.res and i == n - 1:
+                    self.last_issued.arrive()
                 kvb_prev, prev_last = kvb, i == n - 1
                 gi += 1
                 yield
@@ -304,8 +316,18 @@ class DkdvPipeline:
                 yield
 
     # ------------------------------------------------------------ elementwise warps
+    def signal_epi_read(self):
+        """Thread 0 (one of the elementwise threads): the latest epilogue's
+        store has read its staging before epi_read is signalled."""
+        if self.epi_pending:
+            while not all(g[0] for g in self.groups["epilogue"]):
+                yield
+            self.epi_read.arrive()
+            self.epi_pending = False
+
     def elementwise(self):
         gi, epi_last = 0, -3
+        self.epi_pending = False
         for k, n in enumerate(self.units):
             for _ in range(n):
                 b, st, sd = gi % self.nb, gi % self.nqs, gi % 3
@@ -324,6 +346,7 @@ class DkdvPipeline:
                 self.P[b] = ["PdS", gi, False]
                 self.p_full[b].arrive()
                 if self.atomic:
+                    yield from self.signal_epi_read()
                     if gi >= 3:
                         yield from self.wait(self.dq_full[sd], (gi - 3) // 3, "elem.dq_full")
                     if self.res and gi - epi_last <= 2:
@@ -339,6 +362,7 @@ class DkdvPipeline:
             # epilogue: read dV, dK; resident CTAs stage them in dS^T tiles
             last = gi - 1
             yield from self.wait(self.acc_full, k, "epi.acc_full")
+            yield from self.signal_epi_read()
             if self.res and k > 0:
                 yield from self.wait(self.epi_read, k - 1, "epi.epi_read")
             if self.res and self.atomic:
@@ -370,12 +394,14 @@ class DkdvPipeline:
                     self.stored.append(group[2])
                 self.copies.append(read)
                 self.after_read.append((group, complete))
-
-                def store_issuer():  # one thread waits for the read, then signals
-                    while not all(g[0] for g in self.groups["epilogue"]):
-                        yield
-                    self.epi_read.arrive()
-                self.spawned.append(store_issuer())
+                if self.independent_signal:
+                    def signaller():
+                        while not all(g[0] for g in self.groups["epilogue"]):
+                            yield
+                        self.epi_read.arrive()
+                    self.spawned.append(signaller())
+                else:
+                    self.epi_pending = True  # signalled before the next wait on epi_read
             else:
                 self.stored.append(k)
             epi_last = last
@@ -439,10 +465,10 @@ CONFIGS = [(3, True, True, True), (3, True, False, True), (3, False, True, True)
 
 # Tiles per unit of a resident CTA's units (a one-unit CTA takes the first).
 UNIT_PATTERNS = [[1], [2], [3], [4], [8], [1, 1, 1, 1, 1], [2, 1, 3, 1, 1, 2], [8, 8, 8],
-                 [16, 14, 12, 2, 4, 6], [5, 1, 1, 7], [3, 3, 3, 3], [1, 2], [4, 1]]
+                 [16, 14, 12, 2, 4, 6], [5, 1, 1, 7], [3, 3, 3, 3], [1, 2], [4, 1], [1] * 8]
 
 
-def run_case(units, config, seed, skip=frozenset()):
+def run_case(units, config, seed, skip=frozenset(), independent_signal=False):
     buffers, resident, atomic_dq, d64 = config
     DkdvPipeline(units if resident else units[:1], buffers, resident, atomic_dq, d64, seed,
-                 skip).run()
+                 skip, independent_signal).run()
