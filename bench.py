@@ -747,10 +747,12 @@ def run_ours(args, w):
                  "bwd_dq": 0.6 * bwd_f}.get(dom)
     if dom_flops is not None:
         achieved = dom_flops / (per_kernel[dom] * 1e-3) / 1e12
+        # the deterministic dK/dV kernel (no dQ) is another kernel with its own traffic
+        traffic_key = "bwd_dkdv_deterministic" if det and dom == "bwd_dkdv" else dom
         roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sust,
                     "unit": "TFLOP/s", "frac": achieved / peak_sust,
                     "peak_source": f"{pk['source']} bf16 sustained",
-                    "traffic": recorded_traffic(dom, w.name)}
+                    "traffic": recorded_traffic(traffic_key, w.name)}
     else:  # an elementwise kernel dominating would be HBM bound
         roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm"],
                     "unit": "GB/s", "frac": None, "traffic": None}

@@ -217,9 +217,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const long long G = gridDim.x, c = blockIdx.x;
     return k * G + ((k & 1) ? G - 1 - c : c);
   };
+  // (32-bit division when the unit count allows: a 64-bit one is a long
+  // instruction sequence, and every role decodes each unit)
+  const bool units32 = n_units <= 0xffffffffLL;
   auto decode = [&](long long u, FwdUnit& w) {
-    w.bh = static_cast<int>(p.tile_major ? u % p.BH : u / n_pairs);
-    const int idx = static_cast<int>(p.tile_major ? u / p.BH : u % n_pairs);
+    int idx;
+    if (units32) {
+      const uint32_t u32 = static_cast<uint32_t>(u);
+      const uint32_t d = static_cast<uint32_t>(p.tile_major ? p.BH : n_pairs);
+      const uint32_t q = u32 / d, rem = u32 - q * d;
+      w.bh = static_cast<int>(p.tile_major ? rem : q);
+      idx = static_cast<int>(p.tile_major ? q : rem);
+    } else {
+      w.bh = static_cast<int>(p.tile_major ? u % p.BH : u / n_pairs);
+      idx = static_cast<int>(p.tile_major ? u / p.BH : u % n_pairs);
+    }
     w.hh = w.bh % p.H;
     w.bb = w.bh / p.H;
     w.pt = later_longer ? n_pairs - 1 - idx : idx;
