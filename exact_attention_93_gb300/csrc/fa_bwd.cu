@@ -340,6 +340,13 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
             if (gi >= kQS &&
                 !mbar_wait(&s.qdo_empty[st], ((gi - kQS) / kQS) & 1, p.err, abort_flag))
               return false;
+            // Atomic mode: buffer 0's first phase completes before the tile
+            // that reuses the buffer lands, so that the buffer warps' wait
+            // for it implies that phase (the drains do for later tiles): a
+            // buffer warp running ahead cannot arrive for tile kNB in place
+            // of a sibling still to arrive for tile 0.
+            if (kAtomicDq && gi == kNB && !mbar_wait(&s.buf_ready[0], 0, p.err, abort_flag))
+              return false;
             const int q0 = qt * kQ64;
             mbar_arrive_expect_tx(&s.qdo_full[st], 2 * kDB * Smem::kQBlock + 2 * kQ64 * 4);
             for (int kb = 0; kb < kDB; ++kb) {
@@ -550,6 +557,14 @@ __global__ void __launch_bounds__(kPipeThreads<D>, 1)
         if (!warp_wait(&s.qdo_full[gi % kQS], (gi / kQS) & 1, p.err, abort_flag)) break;
         __syncwarp();
         if (lane == 0) {
+          // Buffer b's previous phase (tile gi - kNB) must be complete
+          // before this warp arrives for tile gi: else a warp running ahead
+          // could complete it in place of a sibling still behind.  (Atomic
+          // mode: implied by the producer's wait before tile kNB and by the
+          // drain waits.  A wait that gives up has set the abort flag, so
+          // every later wait fails.)
+          if (!kAtomicDq && gi >= kNB)
+            mbar_wait(&s.buf_ready[b], ((gi - kNB) / kNB) & 1, p.err, abort_flag);
           mbar_arrive(&s.buf_ready[b]);
           // the first kNB tiles have no dV, dK(gi - kNB) to wait for
           if (gi < kNB && warp == 8) mbar_arrive(&s.buf_ready[b]);

@@ -24,6 +24,8 @@ show that each one is needed.
 """
 import random
 
+from protocol_sched import Chooser
+
 
 class ProtocolError(Exception):
     pass
@@ -50,8 +52,11 @@ class DkdvPipeline:
     (D = 64 only); atomic_dq: dQ^T products and their drain."""
 
     def __init__(self, units, buffers, resident, atomic_dq, d64, seed, skip=frozenset(),
-                 independent_signal=False):
+                 independent_signal=False, slow=frozenset()):
         self.rng = random.Random(seed)
+        # slow: see protocol_sched.Chooser (roles, or the queues "q_score",
+        # "q_grad", "copy")
+        self.chooser = Chooser(self.rng, slow)
         # independent_signal: epi_read signalled by its own role as soon as
         # the store has read its staging, instead of by thread 0 just before
         # the first wait on it (every arrival time the kernel can produce,
@@ -109,6 +114,7 @@ class DkdvPipeline:
                 return
             if bar.phases >= k + 2:
                 raise ProtocolError(f"wait {bar.name} phase {k} aliased ({bar.phases} phases)")
+            self.chooser.blocked()
             yield
 
     # ------------------------------------------------------------ producer
@@ -131,6 +137,11 @@ class DkdvPipeline:
                 st = gi % self.nqs
                 if gi >= self.nqs:
                     yield from self.wait(self.qdo_empty[st], (gi - self.nqs) // self.nqs, "prod.qdo_empty")
+                if self.atomic and gi == self.nb:
+                    # buffer 0's first phase complete before the tile that
+                    # reuses it lands: the buffer warps' wait for that tile
+                    # then implies it (later tiles' drains do)
+                    yield from self.wait(self.buf_ready[0], 0, "prod.buf_ready")
                 self.stage[st] = (gi, False)
 
                 def land_q(st=st, gi=gi):
@@ -291,26 +302,26 @@ class DkdvPipeline:
                 if j >= 1:
                     self.stage_free[(j - 1) & 1].arrive()
 
-        gi = 0
-        for _, n in enumerate(self.units):
-            for _ in range(n):
-                b, j = gi % self.nb, gi - 1 - self.nb
-                drain = self.atomic and j >= 0
-                if drain:
-                    yield from drain_load(j, b)
+        # one loop, as in the kernel: the drains run buffers + 1 tiles behind
+        for gi in range(self.total + (self.nb + 1 if self.atomic else 0)):
+            b, j = gi % self.nb, gi - 1 - self.nb
+            drain = self.atomic and 0 <= j < self.total
+            if drain:
+                yield from drain_load(j, b)
+            if gi < self.total:
                 yield from self.wait(self.qdo_full[gi % self.nqs], gi // self.nqs, "buf.qdo_full")
+                # buffer b's previous phase (tile gi - buffers) complete before
+                # this warp arrives for tile gi, else a fast warp's arrival
+                # could complete it in a slow sibling's place; in atomic mode
+                # the producer's wait (tile buffers) and the drains imply it
+                if gi >= self.nb and not self.atomic:
+                    yield from self.wait(self.buf_ready[b], (gi - self.nb) // self.nb, "buf.buf_ready")
                 self.buf_ready[b].arrive()
                 if gi < self.nb and w == 8:  # no dV, dK(gi - buffers) to commit
                     self.buf_ready[b].arrive()
-                if drain:
-                    yield from drain_add(j)
-                gi += 1
-                yield
-        if self.atomic:
-            for j in range(max(0, gi - 1 - self.nb), gi):
-                yield from drain_load(j, (j + 1) % self.nb)
+            if drain:
                 yield from drain_add(j)
-                yield
+            yield
         if self.atomic and self.d64 and quad == 2:
             while not all(g[1] for g in self.groups["reduce"]):
                 yield
@@ -434,7 +445,7 @@ class DkdvPipeline:
                 choices.append("complete")
             if not choices:
                 raise ProtocolError("deadlock: nothing can run")
-            c = self.rng.choice(choices)
+            c = self.chooser.pick(choices, steps)
             if c in ("q_score", "q_grad"):
                 kind, x = (self.q_score if c == "q_score" else self.q_grad).pop(0)
                 if kind == "mma":
@@ -448,6 +459,7 @@ class DkdvPipeline:
                 self.after_read.remove(entry)
                 entry[1]()
             else:
+                self.chooser.enter(c, steps)
                 try:
                     next(roles[c])
                 except StopIteration:
@@ -468,7 +480,7 @@ UNIT_PATTERNS = [[1], [2], [3], [4], [8], [1, 1, 1, 1, 1], [2, 1, 3, 1, 1, 2], [
                  [16, 14, 12, 2, 4, 6], [5, 1, 1, 7], [3, 3, 3, 3], [1, 2], [4, 1], [1] * 8]
 
 
-def run_case(units, config, seed, skip=frozenset(), independent_signal=False):
+def run_case(units, config, seed, skip=frozenset(), independent_signal=False, slow=frozenset()):
     buffers, resident, atomic_dq, d64 = config
     DkdvPipeline(units if resident else units[:1], buffers, resident, atomic_dq, d64, seed,
-                 skip, independent_signal).run()
+                 skip, independent_signal, slow).run()

@@ -16,6 +16,8 @@ leave out.
 """
 import random
 
+from protocol_sched import Chooser
+
 
 class ProtocolError(Exception):
     pass
@@ -37,8 +39,9 @@ class Barrier:
 class DqPipeline:
     BUFFERS, STAGES = 3, 4
 
-    def __init__(self, n_tiles, seed, skip=frozenset()):
+    def __init__(self, n_tiles, seed, skip=frozenset(), slow=frozenset()):
         self.rng = random.Random(seed)
+        self.chooser = Chooser(self.rng, slow)  # slow: see protocol_sched.Chooser
         self.n, self.skip = n_tiles, set(skip)
         B, nb, ns = Barrier, self.BUFFERS, self.STAGES
         self.q_full = B("q_full", 1)
@@ -68,6 +71,7 @@ class DqPipeline:
                 return
             if bar.phases >= k + 2:
                 raise ProtocolError(f"wait {bar.name} phase {k} aliased ({bar.phases} phases)")
+            self.chooser.blocked()
             yield
 
     def producer(self):
@@ -179,13 +183,14 @@ class DqPipeline:
                                                     ("copy", self.copies)) if q]
             if not choices:
                 raise ProtocolError("deadlock: nothing can run")
-            c = self.rng.choice(choices)
+            c = self.chooser.pick(choices, steps)
             if c in ("q_score", "q_grad"):
                 kind, x = (self.q_score if c == "q_score" else self.q_grad).pop(0)
                 x() if kind == "mma" else x.arrive()
             elif c == "copy":
                 self.copies.pop(self.rng.randrange(len(self.copies)))()
             else:
+                self.chooser.enter(c, steps)
                 try:
                     next(roles[c])
                 except StopIteration:

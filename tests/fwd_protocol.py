@@ -17,6 +17,8 @@ a reader still needs them.  The four warps of a softmax group are one role.
 """
 import random
 
+from protocol_sched import Chooser
+
 
 class ProtocolError(Exception):
     pass
@@ -48,8 +50,9 @@ class FwdPipeline:
     empty range has lo > hi); resident: several units per CTA (each with its
     own O staging); otherwise one unit, staged in its Q tiles."""
 
-    def __init__(self, units, resident, seed, skip=frozenset()):
+    def __init__(self, units, resident, seed, skip=frozenset(), slow=frozenset()):
         self.rng = random.Random(seed)
+        self.chooser = Chooser(self.rng, slow)  # slow: see protocol_sched.Chooser
         self.units, self.res = list(units), resident
         self.nqs = 2 if resident else 1
         self.skip = set(skip)
@@ -96,6 +99,7 @@ class FwdPipeline:
                 return
             if bar.phases >= k + 2:
                 raise ProtocolError(f"wait {bar.name} phase {k} aliased ({bar.phases} phases)")
+            self.chooser.blocked()
             yield
 
     def land(self, slot, content, bar, what):
@@ -290,13 +294,14 @@ class FwdPipeline:
             choices = list(roles) + (["queue"] if self.queue else []) + (["copy"] if self.copies else [])
             if not choices:
                 raise ProtocolError("deadlock: nothing can run")
-            c = self.rng.choice(choices)
+            c = self.chooser.pick(choices, steps)
             if c == "queue":
                 kind, x = self.queue.pop(0)
                 x() if kind == "mma" else x.arrive()
             elif c == "copy":
                 self.copies.pop(self.rng.randrange(len(self.copies)))()
             else:
+                self.chooser.enter(c, steps)
                 try:
                     next(roles[c])
                 except StopIteration:

@@ -2,8 +2,9 @@
 (tests/dkdv_protocol.py): every parity wait within one phase of its barrier
 and no shared buffer read early or overwritten while in use, under random
 interleavings of the roles, the two tensor-core queues and the asynchronous
-copies, for resident and one-unit CTAs at D = 64 and D = 128, with atomic and
-deterministic dQ.  A second test leaves out one wait at a time and checks
+copies (uniform, and with a role starved just as its wait is about to
+pass), for resident and one-unit CTAs at D = 64 and D = 128, with atomic
+and deterministic dQ.  A second test leaves out one wait at a time and checks
 that the model then fails: each wait is needed, and the checks catch its
 absence."""
 import pytest
@@ -13,13 +14,14 @@ from dkdv_protocol import CONFIGS, UNIT_PATTERNS, ProtocolError, run_case
 SEEDS = 6
 
 
+@pytest.mark.parametrize("slow", [(), "blocked"])
 @pytest.mark.parametrize("independent_signal", [False, True])
-def test_protocol_holds_under_random_interleavings(independent_signal):
+def test_protocol_holds_under_random_interleavings(independent_signal, slow):
     runs = 0
     for units in UNIT_PATTERNS:
         for config in CONFIGS:
             for seed in range(SEEDS):
-                run_case(units, config, seed, independent_signal=independent_signal)
+                run_case(units, config, seed, independent_signal=independent_signal, slow=slow)
                 runs += 1
     assert runs == len(UNIT_PATTERNS) * len(CONFIGS) * SEEDS
 
@@ -39,10 +41,10 @@ def test_protocol_holds_under_random_interleavings(independent_signal):
 # for its staging warps and the final drains, without which the model
 # deadlocks or reads a stage never written.
 WAITS = [
-    "prod.kv_empty", "prod.qdo_empty",
+    "prod.kv_empty", "prod.qdo_empty", "prod.buf_ready",
     "score.kv_full", "score.buf_ready",
     "grad.s_read", "grad.p_full", "grad.ds_last",
-    "buf.dq_full", "buf.qdo_full", "buf.stage_free",
+    "buf.dq_full", "buf.qdo_full", "buf.buf_ready", "buf.stage_free",
     "elem.s_full", "elem.dq_full", "elem.epi_read",
     "epi.acc_full", "epi.epi_read",
 ]
@@ -55,10 +57,12 @@ def test_each_wait_is_needed(wait):
     # checked with the signal as an independent role.
     independent = wait.endswith("epi_read")
     for seed in range(40):
-        for units in UNIT_PATTERNS:
-            for config in CONFIGS:
-                try:
-                    run_case(units, config, seed, skip={wait}, independent_signal=independent)
-                except ProtocolError:
-                    return
+        for slow in ((), "blocked"):
+            for units in UNIT_PATTERNS:
+                for config in CONFIGS:
+                    try:
+                        run_case(units, config, seed, skip={wait}, independent_signal=independent,
+                                 slow=slow)
+                    except ProtocolError:
+                        return
     pytest.fail(f"the model passes without {wait}")

@@ -1,7 +1,8 @@
 """The barrier protocol of the forward kernel, on a model of its roles
 (tests/fwd_protocol.py): every parity wait within one phase of its barrier
 and no buffer read early or overwritten while in use, under random
-interleavings, for resident and one-unit CTAs over causal, non-causal,
+interleavings (uniform, and with a role starved just as its wait is about to
+pass), for resident and one-unit CTAs over causal, non-causal,
 windowed and ragged bands.  A second test leaves out one wait at a time and
 checks that the model then fails."""
 import pytest
@@ -20,11 +21,12 @@ def cases():
             yield units, True
 
 
-def test_protocol_holds_under_random_interleavings():
+@pytest.mark.parametrize("slow", [(), "blocked"])
+def test_protocol_holds_under_random_interleavings(slow):
     runs = 0
     for units, resident in cases():
         for seed in range(SEEDS):
-            FwdPipeline(units, resident, seed).run()
+            FwdPipeline(units, resident, seed, slow=slow).run()
             runs += 1
     assert runs > 100
 
@@ -42,9 +44,10 @@ WAITS = ["prod.q_empty", "prod.k_empty", "prod.v_empty",
 @pytest.mark.parametrize("wait", WAITS)
 def test_each_wait_is_needed(wait):
     for seed in range(30):
-        for units, resident in cases():
-            try:
-                FwdPipeline(units, resident, seed, skip={wait}).run()
-            except ProtocolError:
-                return
+        for slow in ((), "blocked"):
+            for units, resident in cases():
+                try:
+                    FwdPipeline(units, resident, seed, skip={wait}, slow=slow).run()
+                except ProtocolError:
+                    return
     pytest.fail(f"the model passes without {wait}")
