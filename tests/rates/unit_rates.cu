@@ -34,10 +34,34 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm volatile("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm volatile("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float cvt_f32_f16(uint32_t x) {  // the low half
+  float y;
+  asm volatile("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+               : "=f"(y) : "r"(x));
+  return y;
+}
+
 // kind 0: ex2.approx.ftz.f32 (one result per lane-instruction)
 // kind 1: cvt.rn.satfinite.e4m3x2.f32 (one instruction converts two values;
 //         counted per instruction)
 // kind 2: cvt.rn.bf16x2.f32 (counted per instruction)
+// kind 3: ex2.approx.f16x2 (counted per instruction: two results)
+// kind 4: cvt.f32.f16 (one result per lane-instruction)
+// kind 5: ex2.approx.ftz.f32 and cvt.rn.f16x2.f32 in alternate chains
+//         (counted per instruction of either kind: near the ex2 rate alone
+//         if both use one unit, higher if they use different ones)
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1) rate_kernel(float seed, unsigned long long* cycles,
                                                           uint32_t* sink) {
@@ -59,6 +83,20 @@ __global__ void __launch_bounds__(kThreads, 1) rate_kernel(float seed, unsigned 
     for (int c = 0; c < kChains; ++c) {
       if constexpr (kKind == 0) {
         x[c] = ex2(x[c]);
+      } else if constexpr (kKind == 3) {
+        // keep the half-precision inputs in a small range: feed back the
+        // result's mantissa bits under a fixed exponent
+        const uint32_t y = ex2_f16x2(__float_as_uint(x[c]));
+        x[c] = __uint_as_float((y & 0x03FF03FFu) | 0x38003800u);
+      } else if constexpr (kKind == 4) {
+        x[c] = cvt_f32_f16((__float_as_uint(x[c]) & 0x03FFu) | 0x3800u) + 0.5f;
+      } else if constexpr (kKind == 5) {
+        if (c & 1) {
+          x[c] = ex2(x[c]);
+        } else {
+          const uint32_t r = cvt_f16x2(x[c], -x[c]);
+          x[c] = __uint_as_float((r & 0x007F00FFu) | 0x3F000000u);
+        }
       } else {
         const uint32_t r = kKind == 1 ? cvt_e4m3x2(x[c], -x[c]) : cvt_bf16x2(x[c], -x[c]);
         // feed the result back so that each conversion waits for the last
@@ -107,9 +145,16 @@ int main() {
   const double ex2_rate = measure<0>(sms);
   const double e4m3_rate = measure<1>(sms);
   const double bf16_rate = measure<2>(sms);
-  if (ex2_rate < 0 || e4m3_rate < 0 || bf16_rate < 0) return 3;
+  const double ex2h_rate = measure<3>(sms);
+  const double f32h_rate = measure<4>(sms);
+  const double mix_rate = measure<5>(sms);
+  if (ex2_rate < 0 || e4m3_rate < 0 || bf16_rate < 0 || ex2h_rate < 0 || f32h_rate < 0 ||
+      mix_rate < 0)
+    return 3;
   printf("{\"sms\": %d, \"ex2_approx_f32_per_clk_sm\": %.2f, "
-         "\"cvt_e4m3x2_f32_instr_per_clk_sm\": %.2f, \"cvt_bf16x2_f32_instr_per_clk_sm\": %.2f}\n",
-         sms, ex2_rate, e4m3_rate, bf16_rate);
+         "\"cvt_e4m3x2_f32_instr_per_clk_sm\": %.2f, \"cvt_bf16x2_f32_instr_per_clk_sm\": %.2f, "
+         "\"ex2_approx_f16x2_instr_per_clk_sm\": %.2f, \"cvt_f32_f16_per_clk_sm\": %.2f, "
+         "\"ex2_f32_with_cvt_f16x2_f32_instr_per_clk_sm\": %.2f}\n",
+         sms, ex2_rate, e4m3_rate, bf16_rate, ex2h_rate, f32h_rate, mix_rate);
   return 0;
 }

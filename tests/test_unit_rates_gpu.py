@@ -2,9 +2,11 @@
 
 The benchmark's exponential-rate ceiling takes ex2.approx.ftz.f32 at 32
 lanes per clock per SM, and the kernels' notes quote the e4m3 and bf16 pair
-conversions' rates and the cycles per tensor-core product of each shape the
-tile kernels issue; these tests measure them on the GPU (standalone programs
-under tests/rates/, compiled here for sm_103a) and print them.
+conversions' rates, the half-precision exponential's and conversions' rates
+(the alternatives for the 8-bit softmax) and the cycles per tensor-core
+product of each shape the tile kernels issue; these tests measure them on
+the GPU (standalone programs under tests/rates/, compiled here for sm_103a)
+and print them.
 """
 import json
 import os
@@ -38,6 +40,8 @@ def test_special_function_rates():
     # the constant the benchmark's exponential ceiling uses
     assert abs(r["ex2_approx_f32_per_clk_sm"] - bench.EX2_PER_CLK_SM) <= 0.1 * bench.EX2_PER_CLK_SM
     assert r["cvt_e4m3x2_f32_instr_per_clk_sm"] > 0 and r["cvt_bf16x2_f32_instr_per_clk_sm"] > 0
+    assert r["ex2_approx_f16x2_instr_per_clk_sm"] > 0 and r["cvt_f32_f16_per_clk_sm"] > 0
+    assert r["ex2_f32_with_cvt_f16x2_f32_instr_per_clk_sm"] > 0
 
 
 def test_tensor_core_product_rates():
