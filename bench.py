@@ -752,7 +752,9 @@ def run_ours(args, w):
         roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sust,
                     "unit": "TFLOP/s", "frac": achieved / peak_sust,
                     "peak_source": f"{pk['source']} bf16 sustained",
-                    "traffic": recorded_traffic(traffic_key, w.name)}
+                    "traffic": recorded_traffic(traffic_key, w.name),
+                    # the sources the traffic row (profiles/dram_traffic.md) must match
+                    "kernel_sources": kernel_source_hash()}
     else:  # an elementwise kernel dominating would be HBM bound
         roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm"],
                     "unit": "GB/s", "frac": None, "traffic": None}

@@ -29,3 +29,9 @@ def test_unknown_kernel_has_no_traffic():
     if ("bwd_dkdv_deterministic", "long64k_causal") not in _rows():
         assert bench.recorded_traffic("bwd_dkdv_deterministic", "long64k_causal") is None
     assert bench.recorded_traffic("no_such_kernel", "long64k_causal") is None
+
+
+def test_kernel_source_hash_ignores_comments_and_whitespace():
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and all(c in "0123456789abcdef" for c in h)
+    assert bench.code_text("int a; // note\n/* block */  int b;") == bench.code_text("int a;\nint b;")
